@@ -1,0 +1,708 @@
+// Host runtime of libscute.so: contexts, layers, adapter registration with the
+// fold rule, the per-call launch plan of the adapted linear layer, the byte
+// model and the timing counters.  See include/scute.h for the contract.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ctx.h"
+
+using namespace scute;
+
+namespace {
+
+scute_status fail(scute_ctx *c, scute_status s, const char *fmt, ...) {
+    if (c) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(c->err, sizeof(c->err), fmt, ap);
+        va_end(ap);
+    }
+    return s;
+}
+
+#define CU_TRY(ctx, expr)                                                                      \
+    do {                                                                                       \
+        cudaError_t _e = (expr);                                                               \
+        if (_e != cudaSuccess) {                                                               \
+            (void)cudaGetLastError();                                                          \
+            if (_e == cudaErrorMemoryAllocation)                                               \
+                return fail(ctx, SCUTE_ERR_OOM, "%s: %s", #expr, cudaGetErrorString(_e));      \
+            return fail(ctx, SCUTE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e));         \
+        }                                                                                      \
+    } while (0)
+
+// Keeps the context's device current for the duration of one API call.
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            if (cudaSetDevice(dev) == cudaSuccess) changed = true;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+bool encode_map(scute_ctx *c, CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * (uint64_t)c->esz};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / c->esz), 64};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = c->encode(m, c->esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+scute_status grow(scute_ctx *c, void **buf, size_t *cols, size_t need_cols, size_t elem_bytes,
+                  size_t rows) {
+    if (need_cols <= *cols) return SCUTE_OK;
+    void *p = nullptr;
+    CU_TRY(c, cudaDeviceSynchronize());
+    CU_TRY(c, cudaMalloc(&p, need_cols * elem_bytes * rows));
+    CU_TRY(c, cudaMemset(p, 0, need_cols * elem_bytes * rows));
+    if (*buf) cudaFree(*buf);
+    *buf = p;
+    *cols = need_cols;
+    return SCUTE_OK;
+}
+
+scute_status remap_workspace(scute_ctx *c) {
+    for (auto &L : c->layers) {
+        if (!L.present) continue;
+        if (!encode_map(c, &L.mapXs, c->xs, (uint64_t)L.kdim, (uint64_t)c->max_tokens))
+            return fail(c, SCUTE_ERR_CUDA, "tensor map for the token operand failed");
+        if (L.rv && !encode_map(c, &L.mapU, c->U, (uint64_t)L.krv, (uint64_t)c->max_tokens))
+            return fail(c, SCUTE_ERR_CUDA, "tensor map for the VeRA intermediate failed");
+    }
+    return SCUTE_OK;
+}
+
+scute_status ensure_tmp(scute_ctx *c, size_t bytes) {
+    if (bytes <= c->tmp_bytes) return SCUTE_OK;
+    CU_TRY(c, cudaDeviceSynchronize());
+    if (c->tmp) cudaFree(c->tmp);
+    c->tmp = nullptr;
+    c->tmp_bytes = 0;
+    CU_TRY(c, cudaMalloc(&c->tmp, bytes));
+    c->tmp_bytes = bytes;
+    return SCUTE_OK;
+}
+
+bool layer_ok(const scute_ctx *c, int layer) {
+    return layer >= 0 && layer < c->max_layers && c->layers[layer].present;
+}
+
+void count_launch(scute_ctx *c, int k) { c->launches += k; }
+
+}  // namespace
+
+extern "C" {
+
+int scute_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char *scute_last_error(const scute_ctx *ctx) { return ctx ? ctx->err : "null context"; }
+
+scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int max_tokens,
+                          int max_adapters, int max_layers) {
+    if (!out) return SCUTE_ERR_ARG;
+    *out = nullptr;
+    if (dtype != SCUTE_BF16 && dtype != SCUTE_FP32) return SCUTE_ERR_DTYPE;
+    if (max_tokens < 1 || max_tokens > SCUTE_MAX_TOKENS || max_adapters < 1 ||
+        max_adapters > SCUTE_MAX_ADAPTERS || max_layers < 1 || max_layers > (1 << 20))
+        return SCUTE_ERR_ARG;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return SCUTE_ERR_NO_DEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return SCUTE_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return SCUTE_ERR_NO_DEVICE;  // kernels are built for sm_103a
+    scute_ctx *c = new scute_ctx();
+    c->err[0] = 0;
+    c->device = device;
+    c->dtype = dtype;
+    c->esz = dtype == SCUTE_BF16 ? 2 : 4;
+    c->max_tokens = max_tokens;
+    c->max_adapters = max_adapters;
+    c->max_layers = max_layers;
+    c->num_sms = prop.multiProcessorCount;
+    c->layers.resize(max_layers);
+    c->adapters.resize(max_adapters);
+    c->h_method.assign(max_adapters, (int8_t)-1);
+    DeviceGuard dg(device);
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        delete c;
+        return SCUTE_ERR_NO_DEVICE;
+    }
+    c->encode = reinterpret_cast<PFN_encodeTiled>(fn);
+    const size_t nslots = (size_t)max_layers * max_adapters;
+    bool ok = cudaMalloc(&c->d_slots, nslots * sizeof(Slot)) == cudaSuccess &&
+              cudaMemset(c->d_slots, 0, nslots * sizeof(Slot)) == cudaSuccess &&
+              cudaMalloc(&c->d_method, max_adapters) == cudaSuccess &&
+              cudaMemset(c->d_method, 0xFF, max_adapters) == cudaSuccess &&
+              cudaMalloc(&c->d_perm, sizeof(int) * max_tokens) == cudaSuccess &&
+              cudaMalloc(&c->d_aid, sizeof(int) * max_tokens) == cudaSuccess &&
+              cudaMalloc(&c->d_seg_start, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
+              cudaMalloc(&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
+              cudaMalloc(&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
+              cudaMemset(c->d_meta, 0, sizeof(IndexMeta)) == cudaSuccess &&
+              cudaMalloc(&c->d_status, sizeof(int)) == cudaSuccess &&
+              cudaMemset(c->d_status, 0, sizeof(int)) == cudaSuccess &&
+              cudaMalloc(&c->d_err, sizeof(int)) == cudaSuccess &&
+              cudaMalloc(&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
+              cudaMalloc(&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess;
+    if (!ok) {
+        scute_destroy(c);
+        return SCUTE_ERR_OOM;
+    }
+    *out = c;
+    return SCUTE_OK;
+}
+
+void scute_destroy(scute_ctx *c) {
+    if (!c) return;
+    DeviceGuard dg(c->device);
+    cudaDeviceSynchronize();
+    for (auto &L : c->layers) {
+        if (L.Wt) cudaFree(L.Wt);
+        if (L.Ash) cudaFree(L.Ash);
+        if (L.Bsh) cudaFree(L.Bsh);
+    }
+    for (auto &a : c->adapters)
+        if (a.storage) cudaFree(a.storage);
+    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid,
+                    c->d_meta, c->d_status, c->d_err, c->v_part, c->xs, c->U, c->st_x,
+                    c->st_out, c->st_ids, c->tmp};
+    for (void *p : bufs)
+        if (p) cudaFree(p);
+    if (c->ev_made)
+        for (int i = 0; i < SCUTE_TIMING_SLOTS; ++i) {
+            cudaEventDestroy(c->ev[i][0]);
+            cudaEventDestroy(c->ev[i][1]);
+        }
+    delete c;
+}
+
+scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const void *W) {
+    if (!c || !W) return fail(c, SCUTE_ERR_ARG, "null argument");
+    if (layer < 0 || layer >= c->max_layers) return fail(c, SCUTE_ERR_ARG, "layer id %d out of range", layer);
+    if (c->layers[layer].present) return fail(c, SCUTE_ERR_ARG, "layer %d already exists", layer);
+    if (d_in <= 0 || d_out <= 0 || d_in % 32 || d_out % 32)
+        return fail(c, SCUTE_ERR_SHAPE, "d_in and d_out must be positive multiples of 32");
+    DeviceGuard dg(c->device);
+    const bool f32 = c->dtype == SCUTE_FP32;
+    LayerRec L;
+    L.present = true;
+    L.d_in = d_in;
+    L.d_out = d_out;
+    L.kdim = f32 ? 3 * d_in : d_in;
+    scute_status st = ensure_tmp(c, (size_t)d_in * d_out * c->esz);
+    if (st) return st;
+    CU_TRY(c, cudaMalloc(&L.Wt, (size_t)d_out * L.kdim * c->esz));
+    CU_TRY(c, cudaMemcpy(c->tmp, W, (size_t)d_in * d_out * c->esz, cudaMemcpyDefault));
+    CU_TRY(c, launch_transpose_w(f32, c->tmp, d_in, d_out, L.Wt, L.kdim, f32 ? 1 : 0, 0));
+    CU_TRY(c, cudaDeviceSynchronize());
+    if (!encode_map(c, &L.mapW, L.Wt, (uint64_t)L.kdim, (uint64_t)d_out)) {
+        cudaFree(L.Wt);
+        return fail(c, SCUTE_ERR_CUDA, "tensor map for W failed");
+    }
+    c->layers[layer] = L;
+    // workspace: token operand, host-call staging
+    const size_t old_xs = c->xs_cols;
+    st = grow(c, &c->xs, &c->xs_cols, (size_t)L.kdim, c->esz, c->max_tokens);
+    if (!st) st = grow(c, &c->st_x, &c->st_x_cols, (size_t)d_in, c->esz, c->max_tokens);
+    if (!st) st = grow(c, &c->st_out, &c->st_out_cols, (size_t)d_out, 4, c->max_tokens);
+    if (st) {
+        cudaFree(c->layers[layer].Wt);
+        c->layers[layer] = LayerRec();
+        return st;
+    }
+    (void)old_xs;
+    return remap_workspace(c);
+}
+
+scute_status scute_set_shared(scute_ctx *c, int layer, int rank, const void *A_sh, const void *B_sh) {
+    if (!c || !A_sh || !B_sh) return fail(c, SCUTE_ERR_ARG, "null argument");
+    if (!layer_ok(c, layer)) return fail(c, SCUTE_ERR_ARG, "unknown layer %d", layer);
+    if (rank <= 0 || rank % 32 || rank > SCUTE_MAX_SHARED_RANK)
+        return fail(c, SCUTE_ERR_SHAPE, "shared rank must be a positive multiple of 32, at most %d",
+                    SCUTE_MAX_SHARED_RANK);
+    LayerRec &L = c->layers[layer];
+    if (L.rv) return fail(c, SCUTE_ERR_ARG, "layer %d already has a shared pair", layer);
+    DeviceGuard dg(c->device);
+    const bool f32 = c->dtype == SCUTE_FP32;
+    const int krv = f32 ? 3 * rank : rank;
+    size_t big = (size_t)L.d_in * rank;
+    if ((size_t)rank * L.d_out > big) big = (size_t)rank * L.d_out;
+    scute_status st = ensure_tmp(c, big * c->esz);
+    if (st) return st;
+    void *Ash = nullptr, *Bsh = nullptr;
+    CU_TRY(c, cudaMalloc(&Ash, (size_t)rank * L.kdim * c->esz));
+    CU_TRY(c, cudaMalloc(&Bsh, (size_t)L.d_out * krv * c->esz));
+    CU_TRY(c, cudaMemcpy(c->tmp, A_sh, (size_t)L.d_in * rank * c->esz, cudaMemcpyDefault));
+    CU_TRY(c, launch_transpose_w(f32, c->tmp, L.d_in, rank, Ash, L.kdim, f32 ? 1 : 0, 0));
+    CU_TRY(c, cudaDeviceSynchronize());
+    CU_TRY(c, cudaMemcpy(c->tmp, B_sh, (size_t)rank * L.d_out * c->esz, cudaMemcpyDefault));
+    CU_TRY(c, launch_transpose_w(f32, c->tmp, rank, L.d_out, Bsh, krv, f32 ? 1 : 0, 0));
+    CU_TRY(c, cudaDeviceSynchronize());
+    if (!encode_map(c, &L.mapAsh, Ash, (uint64_t)L.kdim, (uint64_t)rank) ||
+        !encode_map(c, &L.mapBsh, Bsh, (uint64_t)krv, (uint64_t)L.d_out)) {
+        cudaFree(Ash);
+        cudaFree(Bsh);
+        return fail(c, SCUTE_ERR_CUDA, "tensor map for the shared pair failed");
+    }
+    L.Ash = Ash;
+    L.Bsh = Bsh;
+    L.rv = rank;
+    L.krv = krv;
+    st = grow(c, &c->U, &c->u_cols, (size_t)krv, c->esz, c->max_tokens);
+    if (st) return st;
+    return remap_workspace(c);
+}
+
+scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scute_layer_tensors *t,
+                                    int n_layers, int32_t *id_out) {
+    if (!c || !id_out || n_layers < 0 || (n_layers > 0 && !t)) return fail(c, SCUTE_ERR_ARG, "null argument");
+    if (method < SCUTE_LORA || method > SCUTE_NF) return fail(c, SCUTE_ERR_ARG, "bad method %d", (int)method);
+    int id = -1;
+    for (int i = 0; i < c->max_adapters; ++i)
+        if (!c->adapters[i].used) { id = i; break; }
+    if (id < 0) return fail(c, SCUTE_ERR_ARG, "no free adapter id (max_adapters = %d)", c->max_adapters);
+    const bool f32 = c->dtype == SCUTE_FP32;
+    const size_t E = c->esz;
+
+    // ---- validate and size
+    size_t total = 0, tmp_need = 0;
+    std::vector<AdapterLayer> info;
+    for (int i = 0; i < n_layers; ++i) {
+        const scute_layer_tensors &x = t[i];
+        if (!layer_ok(c, x.layer)) return fail(c, SCUTE_ERR_ARG, "unknown layer %d", x.layer);
+        for (int k = 0; k < i; ++k)
+            if (t[k].layer == x.layer) return fail(c, SCUTE_ERR_ARG, "layer %d listed twice", x.layer);
+        const LayerRec &L = c->layers[x.layer];
+        AdapterLayer al{x.layer, 0, false, false, false, false, false};
+        const bool owned = x.A || x.B;
+        switch (method) {
+            case SCUTE_LORA:
+            case SCUTE_DORA:
+                if (!x.A || !x.B) return fail(c, SCUTE_ERR_ARG, "LoRA/DoRA need A and B");
+                if (method == SCUTE_DORA && !x.magnitude) return fail(c, SCUTE_ERR_ARG, "DoRA needs magnitude");
+                al.rank = x.rank;
+                al.s = method == SCUTE_DORA;
+                break;
+            case SCUTE_IA3:
+                if (!x.l) return fail(c, SCUTE_ERR_ARG, "(IA)^3 needs l");
+                al.s = true;
+                break;
+            case SCUTE_VERA:
+                if (!x.d) return fail(c, SCUTE_ERR_ARG, "VeRA needs d");
+                if (!L.rv) return fail(c, SCUTE_ERR_ARG, "layer %d has no shared VeRA pair", x.layer);
+                al.vera = true;
+                al.vera_e = x.e != nullptr;
+                break;
+            case SCUTE_OFT:
+                if (!x.R) return fail(c, SCUTE_ERR_ARG, "OFT needs R");
+                al.R = true;
+                break;
+            case SCUTE_NF:
+                if (owned && (!x.A || !x.B)) return fail(c, SCUTE_ERR_ARG, "an owned term needs A and B");
+                al.rank = owned ? x.rank : 0;
+                al.s = x.s != nullptr;
+                al.b = x.b != nullptr;
+                al.R = x.R != nullptr;
+                break;
+        }
+        if (al.rank < 0 || ((method == SCUTE_LORA || method == SCUTE_DORA || (method == SCUTE_NF && owned)) &&
+                            al.rank < 1))
+            return fail(c, SCUTE_ERR_SHAPE, "rank must be positive");
+        if (al.rank > SCUTE_MAX_RANK)
+            return fail(c, SCUTE_ERR_UNSUPPORTED, "rank %d above %d", al.rank, SCUTE_MAX_RANK);
+        if (al.s) total += align256(4 * (size_t)L.d_out);
+        if (al.b) total += align256(4 * (size_t)L.d_out);
+        if (al.R) total += align256((size_t)L.d_in * OFT_BLK * E);
+        if (al.rank) {
+            total += align256((size_t)al.rank * L.d_in * E) + align256((size_t)al.rank * L.d_out * E);
+            size_t need = align256((size_t)L.d_in * al.rank * E) + align256((size_t)al.rank * L.d_out * E) +
+                          3 * align256(4 * (size_t)L.d_out) + align256(4 * (size_t)al.rank);
+            if (need > tmp_need) tmp_need = need;
+        }
+        if (al.vera) {
+            total += align256(4 * (size_t)L.rv) + align256(4 * (size_t)L.d_out);
+            if (align256(4 * (size_t)L.rv) > tmp_need) tmp_need = align256(4 * (size_t)L.rv);
+        }
+        info.push_back(al);
+    }
+    DeviceGuard dg(c->device);
+    scute_status st = ensure_tmp(c, tmp_need ? tmp_need : 256);
+    if (st) return st;
+    void *storage = nullptr;
+    CU_TRY(c, cudaMalloc(&storage, total ? total : 256));
+    uint8_t *cur = reinterpret_cast<uint8_t *>(storage);
+    auto take = [&](size_t bytes) {
+        void *p = cur;
+        cur += align256(bytes);
+        return p;
+    };
+#define REG_TRY(expr)                                                                  \
+    do {                                                                               \
+        cudaError_t _e = (expr);                                                       \
+        if (_e != cudaSuccess) {                                                       \
+            cudaFree(storage);                                                         \
+            return fail(c, SCUTE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e));   \
+        }                                                                              \
+    } while (0)
+    REG_TRY(cudaMemset(c->d_err, 0, sizeof(int)));
+    std::vector<Slot> slots((size_t)n_layers);
+    for (int i = 0; i < n_layers; ++i) {
+        const scute_layer_tensors &x = t[i];
+        const LayerRec &L = c->layers[x.layer];
+        const AdapterLayer &al = info[i];
+        Slot s{};
+        uint8_t *tmp = reinterpret_cast<uint8_t *>(c->tmp);
+        if (al.rank) {
+            void *tA = tmp;
+            void *tB = tmp + align256((size_t)L.d_in * al.rank * E);
+            float *tv = reinterpret_cast<float *>(tmp + align256((size_t)L.d_in * al.rank * E) +
+                                                  align256((size_t)al.rank * L.d_out * E));
+            float *te = tv + align256(4 * (size_t)L.d_out) / 4;
+            float *tm = te + align256(4 * (size_t)L.d_out) / 4;
+            float *td = tm + align256(4 * (size_t)L.d_out) / 4;
+            REG_TRY(cudaMemcpy(tA, x.A, (size_t)L.d_in * al.rank * E, cudaMemcpyDefault));
+            REG_TRY(cudaMemcpy(tB, x.B, (size_t)al.rank * L.d_out * E, cudaMemcpyDefault));
+            const float *dvec = nullptr, *evec = nullptr, *svec = nullptr;
+            if (method == SCUTE_NF && x.d) {
+                REG_TRY(cudaMemcpy(td, x.d, 4 * (size_t)al.rank, cudaMemcpyDefault));
+                dvec = td;
+            }
+            if (method == SCUTE_NF && x.e) {
+                REG_TRY(cudaMemcpy(te, x.e, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+                evec = te;
+            }
+            void *Ap = take((size_t)al.rank * L.d_in * E);
+            void *Bp = take((size_t)al.rank * L.d_out * E);
+            if (method == SCUTE_DORA) {
+                float *sp = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
+                REG_TRY(cudaMemcpy(tm, x.magnitude, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+                REG_TRY(launch_dora_scale(f32, L.Wt, L.kdim, L.d_in, L.d_out, tA, tB, al.rank, x.c, tm, sp,
+                                          c->d_err, 0));
+                s.s = sp;
+                svec = sp;
+            }
+            REG_TRY(launch_fold_A(f32, tA, L.d_in, al.rank, x.c, dvec, Ap, 0));
+            REG_TRY(launch_fold_B(f32, tB, al.rank, L.d_out, evec, svec, Bp, 0));
+            s.A = Ap;
+            s.B = Bp;
+            s.rank = al.rank;
+        }
+        if (method == SCUTE_IA3) {
+            float *sp = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
+            REG_TRY(cudaMemcpy(sp, x.l, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+            s.s = sp;
+        }
+        if (method == SCUTE_NF && x.s) {
+            float *sp = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
+            REG_TRY(cudaMemcpy(sp, x.s, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+            s.s = sp;
+        }
+        if (method == SCUTE_NF && x.b) {
+            float *bp = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
+            REG_TRY(cudaMemcpy(bp, x.b, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+            s.b = bp;
+        }
+        if (al.R) {
+            void *Rp = take((size_t)L.d_in * OFT_BLK * E);
+            REG_TRY(cudaMemcpy(Rp, x.R, (size_t)L.d_in * OFT_BLK * E, cudaMemcpyDefault));
+            s.R = Rp;
+        }
+        if (al.vera) {
+            float *dp = reinterpret_cast<float *>(take(4 * (size_t)L.rv));
+            float *ep = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
+            float *td = reinterpret_cast<float *>(tmp);
+            REG_TRY(cudaMemcpy(td, x.d, 4 * (size_t)L.rv, cudaMemcpyDefault));
+            // the shared term's scalar c is the adapter's own: merged into its d
+            REG_TRY(launch_scale_vec(td, x.c == 0.f ? 1.f : x.c, dp, L.rv, 0));
+            if (x.e) {
+                REG_TRY(cudaMemcpy(ep, x.e, 4 * (size_t)L.d_out, cudaMemcpyDefault));
+                s.ve = ep;
+            }
+            s.vd = dp;
+        }
+        // raw tensors in tmp are reused by the next layer: finish this one first
+        REG_TRY(cudaDeviceSynchronize());
+        slots[i] = s;
+    }
+    int herr = 0;
+    REG_TRY(cudaMemcpy(&herr, c->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (herr) {
+        cudaFree(storage);
+        return fail(c, SCUTE_ERR_ARG, "DoRA: a column of W + cAB has zero norm");
+    }
+    for (int i = 0; i < n_layers; ++i)
+        REG_TRY(cudaMemcpy(c->d_slots + (size_t)t[i].layer * c->max_adapters + id, &slots[i], sizeof(Slot),
+                           cudaMemcpyHostToDevice));
+    const int8_t m8 = (int8_t)method;
+    REG_TRY(cudaMemcpy(c->d_method + id, &m8, 1, cudaMemcpyHostToDevice));
+#undef REG_TRY
+    AdapterRec &a = c->adapters[id];
+    a.used = true;
+    a.method = method;
+    a.storage = storage;
+    a.layers = info;
+    c->h_method[id] = m8;
+    for (const auto &al : info) {
+        LayerRec &L = c->layers[al.layer];
+        if (al.rank) ++L.n_lr;
+        if (al.vera) ++L.n_vera;
+        if (al.R) ++L.n_rot;
+    }
+    *id_out = id;
+    return SCUTE_OK;
+}
+
+scute_status scute_unregister_adapter(scute_ctx *c, int32_t id) {
+    if (!c) return SCUTE_ERR_ARG;
+    if (id < 0 || id >= c->max_adapters || !c->adapters[id].used)
+        return fail(c, SCUTE_ERR_ARG, "adapter %d is not registered", id);
+    DeviceGuard dg(c->device);
+    CU_TRY(c, cudaDeviceSynchronize());
+    AdapterRec &a = c->adapters[id];
+    const int8_t none = -1;
+    CU_TRY(c, cudaMemcpy(c->d_method + id, &none, 1, cudaMemcpyHostToDevice));
+    const Slot zero{};
+    for (const auto &al : a.layers) {
+        CU_TRY(c, cudaMemcpy(c->d_slots + (size_t)al.layer * c->max_adapters + id, &zero, sizeof(Slot),
+                             cudaMemcpyHostToDevice));
+        LayerRec &L = c->layers[al.layer];
+        if (al.rank) --L.n_lr;
+        if (al.vera) --L.n_vera;
+        if (al.R) --L.n_rot;
+    }
+    CU_TRY(c, cudaFree(a.storage));
+    a = AdapterRec();
+    c->h_method[id] = -1;
+    return SCUTE_OK;
+}
+
+static int max_owned_rank(const scute_ctx *c, int layer) {
+    int r = 0;
+    for (const auto &a : c->adapters)
+        if (a.used)
+            for (const auto &al : a.layers)
+                if (al.layer == layer && al.rank > r) r = al.rank;
+    return r;
+}
+
+scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64_t n, int layer, void *out,
+                          scute_dtype out_dtype, void *stream) {
+    if (!c) return SCUTE_ERR_ARG;
+    if (!layer_ok(c, layer)) return fail(c, SCUTE_ERR_ARG, "unknown layer %d", layer);
+    if (n < 0 || n > c->max_tokens) return fail(c, SCUTE_ERR_ARG, "n = %lld outside 0..%d", (long long)n, c->max_tokens);
+    if (out_dtype != SCUTE_BF16 && out_dtype != SCUTE_FP32) return fail(c, SCUTE_ERR_DTYPE, "bad out dtype");
+    if (c->dtype == SCUTE_FP32 && out_dtype != SCUTE_FP32)
+        return fail(c, SCUTE_ERR_DTYPE, "an fp32 context writes fp32 output");
+    if (n == 0) return SCUTE_OK;
+    if (!x || !ids || !out) return fail(c, SCUTE_ERR_ARG, "null argument");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return fail(c, SCUTE_ERR_ARG, "x and out must be 16-byte aligned");
+    DeviceGuard dg(c->device);
+    const LayerRec &L = c->layers[layer];
+    const bool f32 = c->dtype == SCUTE_FP32;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int nn = (int)n;
+    const Slot *slots = c->d_slots + (size_t)layer * c->max_adapters;
+    const int out_f32 = out_dtype == SCUTE_FP32 ? 1 : 0;
+    int k = 0;
+
+    // 1. token indexing
+    CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
+                           c->d_seg_aid, c->d_meta, c->d_status, st));
+    ++k;
+    // 2. rotation prologue into the sorted token operand
+    CU_TRY(c, launch_gather_rotate(f32, x, L.d_in, nn, c->d_perm, c->d_aid, slots, c->xs, L.kdim, st, c->pdl));
+    ++k;
+    // 3. base GEMM with the s / b epilogue
+    const bool tok_on_p = nn > 256;
+    GemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.mapP = tok_on_p ? L.mapXs : L.mapW;
+    g.mapQ = tok_on_p ? L.mapW : L.mapXs;
+    g.kblocks = (L.kdim * c->esz + 127) / 128;
+    g.n_feat = L.d_out;
+    g.tok_on_p = tok_on_p ? 1 : 0;
+    g.n_tok_host = nn;
+    g.epi = EPI_BASE;
+    g.out_f32 = out_f32;
+    g.ld_out = L.d_out;
+    g.slots = slots;
+    g.perm = c->d_perm;
+    g.aid_s = c->d_aid;
+    g.out = out;
+    g.status = c->d_status;
+    GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms);
+    g.splits = p.splits;
+    g.stages = p.stages;
+    g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
+    const int slot = c->t_next;
+    if (c->timing) CU_TRY(c, cudaEventRecord(c->ev[slot][0], st));
+    CU_TRY(c, launch_gemm(g, p, st, c->pdl));
+    if (c->timing) {
+        CU_TRY(c, cudaEventRecord(c->ev[slot][1], st));
+        c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
+        if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
+    }
+    ++k;
+    // 4. owned low-rank shrink / expand
+    if (L.n_lr > 0) {
+        int bound = nn;
+        int reg = 0;
+        for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
+        if (reg + 1 < bound) bound = reg + 1;
+        CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, nn, bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
+                                 c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
+                                 max_owned_rank(c, layer)));
+        k += 2;
+    }
+    // 5. VeRA: shared shrink then shared expand over the VeRA rows only
+    if (L.rv > 0 && L.n_vera > 0) {
+        GemmArgs v;
+        memset(&v, 0, sizeof(v));
+        v.mapP = tok_on_p ? L.mapXs : L.mapAsh;
+        v.mapQ = tok_on_p ? L.mapAsh : L.mapXs;
+        v.kblocks = g.kblocks;
+        v.n_feat = L.rv;
+        v.tok_on_p = g.tok_on_p;
+        v.n_tok_host = nn;
+        v.tok_cnt = &c->d_meta->count[RANK_VERA];
+        v.tok_base = &c->d_meta->offset[RANK_VERA];
+        v.sorted_base = &c->d_meta->offset[RANK_VERA];
+        v.epi = EPI_VERA_D;
+        v.ldu = L.krv;
+        v.u_split3 = f32 ? 1 : 0;
+        v.u_rank = L.rv;
+        v.slots = slots;
+        v.perm = c->d_perm;
+        v.aid_s = c->d_aid;
+        v.U = c->U;
+        v.status = c->d_status;
+        GemmPlan pv = plan_gemm(nn, L.rv, v.kblocks, tok_on_p, f32, c->num_sms);
+        v.splits = pv.splits;
+        v.stages = pv.stages;
+        v.n_ft = tok_on_p ? (L.rv + pv.bn - 1) / pv.bn : (L.rv + 127) / 128;
+        CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
+
+        GemmArgs e = v;
+        e.mapP = tok_on_p ? L.mapU : L.mapBsh;
+        e.mapQ = tok_on_p ? L.mapBsh : L.mapU;
+        e.kblocks = (L.krv * c->esz + 127) / 128;
+        e.n_feat = L.d_out;
+        e.tok_base = nullptr;
+        e.epi = EPI_VERA_E;
+        e.out = out;
+        e.out_f32 = out_f32;
+        e.ld_out = L.d_out;
+        GemmPlan pe = plan_gemm(nn, L.d_out, e.kblocks, tok_on_p, f32, c->num_sms);
+        e.splits = pe.splits;
+        e.stages = pe.stages;
+        e.n_ft = tok_on_p ? (L.d_out + pe.bn - 1) / pe.bn : (L.d_out + 127) / 128;
+        CU_TRY(c, launch_gemm(e, pe, st, c->pdl));
+        k += 2;
+    }
+    count_launch(c, k);
+    return SCUTE_OK;
+}
+
+scute_status scute_linear_host(scute_ctx *c, const void *x_host, const int32_t *ids_host, int64_t n, int layer,
+                               void *out_host, scute_dtype out_dtype, void *stream) {
+    if (!c) return SCUTE_ERR_ARG;
+    if (!layer_ok(c, layer)) return fail(c, SCUTE_ERR_ARG, "unknown layer %d", layer);
+    if (n < 0 || n > c->max_tokens) return fail(c, SCUTE_ERR_ARG, "n out of range");
+    if (n == 0) return SCUTE_OK;
+    if (!x_host || !ids_host || !out_host) return fail(c, SCUTE_ERR_ARG, "null argument");
+    DeviceGuard dg(c->device);
+    const LayerRec &L = c->layers[layer];
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t osz = out_dtype == SCUTE_FP32 ? 4 : 2;
+    CU_TRY(c, cudaMemcpyAsync(c->st_x, x_host, (size_t)n * L.d_in * c->esz, cudaMemcpyHostToDevice, st));
+    CU_TRY(c, cudaMemcpyAsync(c->st_ids, ids_host, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+    scute_status s = scute_linear(c, c->st_x, c->st_ids, n, layer, c->st_out, out_dtype, stream);
+    if (s) return s;
+    CU_TRY(c, cudaMemcpyAsync(out_host, c->st_out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost, st));
+    return SCUTE_OK;
+}
+
+scute_status scute_sync_status(scute_ctx *c) {
+    if (!c) return SCUTE_ERR_ARG;
+    DeviceGuard dg(c->device);
+    CU_TRY(c, cudaDeviceSynchronize());
+    int s = 0;
+    CU_TRY(c, cudaMemcpy(&s, c->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    CU_TRY(c, cudaMemset(c->d_status, 0, sizeof(int)));
+    if (s & STATUS_TIMEOUT) return fail(c, SCUTE_ERR_TIMEOUT, "a device-side wait timed out");
+    if (s & STATUS_BAD_ADAPTER) return fail(c, SCUTE_ERR_BAD_ADAPTER, "a token id named no registered adapter");
+    return SCUTE_OK;
+}
+
+scute_status scute_debug_index(scute_ctx *c, const int32_t *ids, int64_t n, int32_t *perm, int32_t *aid_sorted,
+                               int32_t *seg_start, int32_t *seg_aid, int32_t *counts, void *stream) {
+    if (!c || (n > 0 && (!ids || !perm || !aid_sorted || !seg_aid)) || !seg_start || !counts)
+        return fail(c, SCUTE_ERR_ARG, "null argument");
+    if (n < 0 || n > c->max_tokens) return fail(c, SCUTE_ERR_ARG, "n out of range");
+    DeviceGuard dg(c->device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    CU_TRY(c, launch_index(ids, (int)n, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
+                           c->d_seg_aid, c->d_meta, c->d_status, st));
+    count_launch(c, 1);
+    if (n > 0) {
+        CU_TRY(c, cudaMemcpyAsync(perm, c->d_perm, 4 * (size_t)n, cudaMemcpyDeviceToDevice, st));
+        CU_TRY(c, cudaMemcpyAsync(aid_sorted, c->d_aid, 4 * (size_t)n, cudaMemcpyDeviceToDevice, st));
+        CU_TRY(c, cudaMemcpyAsync(seg_aid, c->d_seg_aid, 4 * (size_t)n, cudaMemcpyDeviceToDevice, st));
+    }
+    CU_TRY(c, cudaMemcpyAsync(seg_start, c->d_seg_start, 4 * (size_t)(n + 1), cudaMemcpyDeviceToDevice, st));
+    CU_TRY(c, cudaMemcpyAsync(counts, c->d_meta, sizeof(IndexMeta), cudaMemcpyDeviceToDevice, st));
+    return SCUTE_OK;
+}
+
+int64_t scute_launch_count(const scute_ctx *c) { return c ? c->launches : 0; }
+
+scute_status scute_timing_enable(scute_ctx *c, int enable) {
+    if (!c) return SCUTE_ERR_ARG;
+    DeviceGuard dg(c->device);
+    if (enable && !c->ev_made) {
+        for (int i = 0; i < SCUTE_TIMING_SLOTS; ++i) {
+            CU_TRY(c, cudaEventCreate(&c->ev[i][0]));
+            CU_TRY(c, cudaEventCreate(&c->ev[i][1]));
+        }
+        c->ev_made = true;
+    }
+    c->timing = enable != 0;
+    return SCUTE_OK;
+}
+
+scute_status scute_timing_reset(scute_ctx *c) {
+    if (!c) return SCUTE_ERR_ARG;
+    c->t_next = 0;
+    c->t_used = 0;
+    return SCUTE_OK;
+}
+
+scute_status scute_timing_read(scute_ctx *c, float *ms, int max, int *n_out) {
+    if (!c || !ms || !n_out) return SCUTE_ERR_ARG;
+    DeviceGuard dg(c->device);
+    CU_TRY(c, cudaDeviceSynchronize());
+    int m = c->t_used < max ? c->t_used : max;
+    for (int i = 0; i < m; ++i) CU_TRY(c, cudaEventElapsedTime(&ms[i], c->ev[i][0], c->ev[i][1]));
+    *n_out = m;
+    return SCUTE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Private definition of the context object shared by the host runtime files.
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "scute.h"
+
+namespace scute {
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct LayerRec {
+    bool present = false;
+    int d_in = 0, d_out = 0, kdim = 0;
+    void *Wt = nullptr;  // [d_out][kdim]
+    CUtensorMap mapW, mapXs;
+    int rv = 0, krv = 0;
+    void *Ash = nullptr;  // [rv][kdim]
+    void *Bsh = nullptr;  // [d_out][krv]
+    CUtensorMap mapAsh, mapBsh, mapU;
+    int n_lr = 0;         // registered adapters with an owned term here
+    int n_vera = 0;       // registered adapters with a VeRA term here
+    int n_rot = 0;        // registered adapters with a rotation here
+};
+
+struct AdapterLayer {
+    int layer;
+    int rank;      // owned rank (0 none)
+    bool s, b, R, vera, vera_e;
+};
+
+struct AdapterRec {
+    bool used = false;
+    int method = -1;
+    void *storage = nullptr;
+    std::vector<AdapterLayer> layers;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace scute
+
+using namespace scute;
+
+struct scute_ctx {
+    int device = 0;
+    scute_dtype dtype = SCUTE_BF16;
+    int esz = 2;
+    int max_tokens = 0, max_adapters = 0, max_layers = 0;
+    int num_sms = 0;
+    bool pdl = true;
+    std::vector<LayerRec> layers;
+    std::vector<AdapterRec> adapters;
+    std::vector<int8_t> h_method;
+    Slot *d_slots = nullptr;
+    int8_t *d_method = nullptr;
+    int *d_perm = nullptr, *d_aid = nullptr, *d_seg_start = nullptr, *d_seg_aid = nullptr;
+    IndexMeta *d_meta = nullptr;
+    int *d_status = nullptr;
+    int *d_err = nullptr;
+    float *v_part = nullptr;
+    void *xs = nullptr;
+    size_t xs_cols = 0;  // elements per row the xs buffer holds
+    void *U = nullptr;
+    size_t u_cols = 0;
+    void *st_x = nullptr, *st_out = nullptr;
+    int32_t *st_ids = nullptr;
+    size_t st_x_cols = 0, st_out_cols = 0;
+    void *tmp = nullptr;
+    size_t tmp_bytes = 0;
+    PFN_encodeTiled encode = nullptr;
+    int64_t launches = 0;
+    bool timing = false;
+    cudaEvent_t ev[SCUTE_TIMING_SLOTS][2];
+    bool ev_made = false;
+    int t_next = 0, t_used = 0;
+    char err[512];
+};
+

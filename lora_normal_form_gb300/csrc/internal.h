@@ -1,0 +1,147 @@
+// Internal declarations shared by the kernels and the host runtime of
+// libscute.so.  Nothing here is part of the C ABI (include/scute.h is).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap type only; the driver entry point is fetched at run time
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace scute {
+
+// Method ranks: the order tokens are grouped in (base-only tokens last).
+enum : int {
+    RANK_LORA = 0, RANK_DORA = 1, RANK_IA3 = 2, RANK_VERA = 3, RANK_OFT = 4, RANK_NF = 5,
+    RANK_BASE = 6, N_RANKS = 7
+};
+
+// Device status word bits (read back by scute_sync_status).
+enum : int { STATUS_BAD_ADAPTER = 1, STATUS_TIMEOUT = 2 };
+
+constexpr int OFT_BLK = 32;
+constexpr int MAX_RANK = 64;          // owned low-rank term
+constexpr int KS_MAX = 8;             // K splits of the low-rank shrink
+constexpr int INDEX_MAX_TOKENS = 16384;
+
+// One (layer, adapter) entry of the device slot table: the folded normal form
+// of that adapter on that layer.  A null pointer is the identity value.
+struct Slot {
+    const float *s;    // [d_out] live column factor (DoRA, (IA)^3, NF)
+    const float *b;    // [d_out] live shift (NF)
+    const void *R;     // [d_in/32][32][32] live input rotation (OFT, NF)
+    const void *A;     // owned A' = c A diag(d), stored [rank][d_in]
+    const void *B;     // owned B' = B diag(e), stored [rank][d_out]
+    const float *vd;   // VeRA d [shared rank] (c folded in); null = no shared term
+    const float *ve;   // VeRA e [d_out]; null = ones
+    int rank;          // rank of the owned term (0 = none)
+    int pad;
+};
+
+// Results of the token indexing kernel beyond the per-row arrays.
+struct IndexMeta {
+    int n_seg;
+    int count[N_RANKS];       // sorted rows per method rank
+    int offset[N_RANKS];      // first sorted row per method rank
+    int seg_count[N_RANKS];   // segments per method rank
+};
+static_assert(sizeof(IndexMeta) == 22 * sizeof(int), "IndexMeta layout");
+
+// ---------------------------------------------------------------- GEMM
+// D[128 x BN] += P[128 rows, K] * Q[BN rows, K]^T on tcgen05, both operands
+// K-major in 128-byte swizzled shared-memory tiles loaded by TMA.
+enum : int { EPI_BASE = 0, EPI_VERA_D = 1, EPI_VERA_E = 2 };
+
+struct GemmArgs {
+    CUtensorMap mapP;          // P operand: 128-row tiles
+    CUtensorMap mapQ;          // Q operand: BN-row tiles
+    int kblocks;               // K extent in 128-byte blocks
+    int n_ft;                  // tiles along the feature dimension
+    int n_feat;                // features (d_out, or the shared rank)
+    int tok_on_p;              // 1: P rows are tokens; 0: Q rows are tokens
+    int n_tok_host;            // token rows when tok_cnt is null (and the grid bound)
+    const int *tok_cnt;        // device token-row count (VeRA rows) or null
+    const int *tok_base;       // device row offset of the token operand's TMA coordinates
+    const int *sorted_base;    // device offset from token row to sorted row
+    int splits;                // K splits = cluster size (1 = persistent tile loop)
+    int stages;                // shared-memory pipeline depth
+    int epi;                   // EPI_*
+    int out_f32;               // output element type (1 float, 0 bf16)
+    int ld_out;                // output row pitch in elements
+    int ldu;                   // U row pitch in elements
+    int u_split3;              // U holds [hi | hi | lo] tf32 parts (fp32 context)
+    int u_rank;                // shared rank (for the split layout)
+    const Slot *slots;         // slot table row of this layer: slots[adapter]
+    const int *perm;           // sorted row -> token
+    const int *aid_s;          // sorted row -> adapter (-1 base)
+    void *out;                 // [n, ld_out]
+    void *U;                   // VeRA intermediate
+    int *status;
+};
+
+struct GemmPlan {
+    int bn;        // 64, 128 or 256
+    int splits;    // 1, 2, 4, 8
+    int stages;
+    int grid;
+    int tf32;
+    size_t smem;
+};
+
+GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms);
+cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl);
+
+// K splits of the owned low-rank shrink: at most KS_MAX chunks of a multiple
+// of 256 elements each.
+inline int lowrank_ks(int d_in, int *kchunk_out) {
+    int ks = (d_in + 511) / 512;
+    if (ks > KS_MAX) ks = KS_MAX;
+    int kchunk = (d_in + ks - 1) / ks;
+    kchunk = (kchunk + 255) / 256 * 256;
+    ks = (d_in + kchunk - 1) / kchunk;
+    if (kchunk_out) *kchunk_out = kchunk;
+    return ks;
+}
+
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum
+// less its static shared memory (asked once per kernel).
+template <typename K>
+cudaError_t allow_max_dynamic_smem(K kernel) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)fa.sharedSizeBytes);
+    return e;
+}
+
+// ---------------------------------------------------------------- other kernels
+cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
+                         int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
+                         int *status, cudaStream_t st);
+
+cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const int *perm,
+                                 const int *aid_s, const Slot *slots, void *xs, int kdim,
+                                 cudaStream_t st, bool pdl);
+
+cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int n, int seg_bound,
+                           const int *perm, const int *seg_start, const int *seg_aid,
+                           const IndexMeta *meta, const Slot *slots, float *v_part,
+                           int max_tokens, void *out, int out_f32, cudaStream_t st, bool pdl,
+                           int max_rank);
+
+// registration-time kernels
+cudaError_t launch_transpose_w(bool f32, const void *W, int rows, int cols, void *Wt, int kdim,
+                               int pattern, cudaStream_t st);
+cudaError_t launch_fold_A(bool f32, const void *A, int d_in, int rank, float c, const float *d,
+                          void *Aout, cudaStream_t st);
+cudaError_t launch_fold_B(bool f32, const void *B, int rank, int d_out, const float *e,
+                          const float *s, void *Bout, cudaStream_t st);
+cudaError_t launch_dora_scale(bool f32, const void *Wt, int kdim, int d_in, int d_out,
+                              const void *A, const void *B, int rank, float c,
+                              const float *m, float *s_out, int *err, cudaStream_t st);
+cudaError_t launch_scale_vec(const float *v, float c, float *out, int n, cudaStream_t st);
+
+}  // namespace scute

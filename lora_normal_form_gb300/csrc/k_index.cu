@@ -1,0 +1,205 @@
+// Token -> segment indexing (one CTA).
+//
+// The batched layer works per adapter segment (article "Scute: Exact Batched
+// Serving for PEFT Adapters Beyond LoRA", paper-daily.com, section "The big
+// picture": shrink and expand per adapter segment; section "Where is the
+// cheapest place to compute the remaining slots?": each tile belongs to one
+// adapter).  This kernel orders the tokens by the key (method, adapter id) with
+// ties kept in token order, so that every method's rows and every adapter's
+// rows are contiguous, and emits:
+//   perm[i]        token of sorted row i
+//   aid_s[i]       adapter of sorted row i (-1 = base only)
+//   seg_start/aid  maximal runs of one key
+//   meta           rows, first row and segments per method
+// Ids that name no registered adapter become base-only rows and set
+// STATUS_BAD_ADAPTER.
+//
+// Sort: each token becomes the 32-bit word (key << 16) | token, sorted by a
+// two-pass least-significant-digit counting sort on the key's two bytes.  A pass
+// is stable: warp w owns a contiguous run of the input, counts digits with
+// __match_any_sync, and scatters in order through per-(warp, digit) offsets laid
+// out digit-major, warp-minor.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace scute {
+
+namespace {
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+// Exclusive scan of one value per thread over the whole block (<= 1024
+// threads).  Returns the exclusive prefix; *total receives the block sum.
+__device__ int block_excl_scan(int v, int *s_warp, int *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int incl = warp_incl_scan(v);
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        const int x = lane < nw ? s_warp[lane] : 0;
+        const int xi = warp_incl_scan(x);
+        if (lane < nw) s_warp[lane] = xi - x;  // exclusive prefix of warp totals
+        if (lane == nw - 1) s_warp[32] = xi;
+    }
+    __syncthreads();
+    const int r = s_warp[w] + incl - v;
+    if (total) *total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+__device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift, int *hist,
+                           int *s_warp) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+    int chunk = (n + nw - 1) / nw;
+    chunk = (chunk + 31) & ~31;
+    const int beg = w * chunk;
+    const int end = min(n, beg + chunk);
+    for (int i = tid; i < nw * 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int base = beg; base < end; base += 32) {
+        const int i = base + lane;
+        const bool valid = i < end;
+        const uint32_t d = valid ? ((src[i] >> shift) & 255u) : (256u + lane);
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (valid && lane == __ffs(peers) - 1) hist[w * 256 + d] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    int tot = 0;
+    if (tid < 256)
+        for (int k = 0; k < nw; ++k) tot += hist[k * 256 + tid];
+    const int excl = block_excl_scan(tid < 256 ? tot : 0, s_warp, nullptr);
+    if (tid < 256) {
+        int run = excl;
+        for (int k = 0; k < nw; ++k) {
+            const int c = hist[k * 256 + tid];
+            hist[k * 256 + tid] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int base = beg; base < end; base += 32) {
+        const int i = base + lane;
+        const bool valid = i < end;
+        const uint32_t v = valid ? src[i] : 0u;
+        const uint32_t d = valid ? ((v >> shift) & 255u) : (256u + lane);
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        int pos = 0;
+        if (valid) pos = hist[w * 256 + d] + __popc(peers & lt);
+        __syncwarp();
+        if (valid) {
+            dst[pos] = v;
+            if (lane == __ffs(peers) - 1) hist[w * 256 + d] += __popc(peers);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, const int8_t *method_tab,
+                                                     int A, int *perm, int *aid_s, int *seg_start,
+                                                     int *seg_aid, IndexMeta *meta, int *status) {
+    extern __shared__ uint32_t sm[];
+    uint32_t *bufA = sm;
+    uint32_t *bufB = sm + n;
+    int *hist = reinterpret_cast<int *>(bufB + n);
+    __shared__ int s_warp[33];
+    __shared__ int s_count[N_RANKS], s_segc[N_RANKS];
+    __shared__ int s_bad;
+
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+    const int tid = threadIdx.x;
+    if (tid == 0) s_bad = 0;
+    if (tid < N_RANKS) { s_count[tid] = 0; s_segc[tid] = 0; }
+    const uint32_t base_key = (uint32_t)RANK_BASE * (uint32_t)A;
+    for (int t = tid; t < n; t += blockDim.x) {
+        const int id = ids[t];
+        int m = -1;
+        if (id >= 0 && id < A) m = method_tab[id];
+        if (m < 0 && id != -1) s_bad = 1;
+        const uint32_t key = m >= 0 ? (uint32_t)m * (uint32_t)A + (uint32_t)id : base_key;
+        bufA[t] = (key << 16) | (uint32_t)t;
+    }
+    __syncthreads();
+    radix_pass(bufA, bufB, n, 16, hist, s_warp);
+    radix_pass(bufB, bufA, n, 24, hist, s_warp);
+
+    // segments: runs of one key; each thread owns a contiguous run of rows
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int r0 = min(n, tid * per), r1 = min(n, r0 + per);
+    int nflag = 0;
+    for (int i = r0; i < r1; ++i) {
+        const uint32_t v = bufA[i];
+        const uint32_t key = v >> 16;
+        const int rank = (int)(key / (uint32_t)A);
+        perm[i] = (int)(v & 0xFFFFu);
+        aid_s[i] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
+        atomicAdd(&s_count[rank], 1);
+        if (i == 0 || (bufA[i - 1] >> 16) != key) ++nflag;
+    }
+    int total = 0;
+    int s = block_excl_scan(nflag, s_warp, &total);
+    for (int i = r0; i < r1; ++i) {
+        const uint32_t key = bufA[i] >> 16;
+        if (i == 0 || (bufA[i - 1] >> 16) != key) {
+            const int rank = (int)(key / (uint32_t)A);
+            seg_start[s] = i;
+            seg_aid[s] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
+            atomicAdd(&s_segc[rank], 1);
+            ++s;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        seg_start[total] = n;
+        meta->n_seg = total;
+        int off = 0;
+        for (int r = 0; r < N_RANKS; ++r) {
+            meta->count[r] = s_count[r];
+            meta->offset[r] = off;
+            meta->seg_count[r] = s_segc[r];
+            off += s_count[r];
+        }
+        if (s_bad) atomicOr(status, STATUS_BAD_ADAPTER);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
+                         int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
+                         int *status, cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = allow_max_dynamic_smem(index_kernel);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int threads = n <= 2048 ? 256 : 1024;
+    const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * 256 * sizeof(int);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, index_kernel, ids, n, method_tab, max_adapters, perm, aid_s,
+                              seg_start, seg_aid, meta, status);
+}
+
+}  // namespace scute

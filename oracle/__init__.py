@@ -15,11 +15,12 @@ cited below as *the article*) says the layer computes, in float64 with NumPy:
 * ``normal_form``  the six-slot normal form, the method -> slot mapping, the
                    fold rule applied at load, and the merged per-adapter weight;
 * ``indexing``     the token -> segment indexing (stable sort by method, id);
-* ``batch``        a heterogeneous batch evaluated row by row group.
+* ``batch``        a heterogeneous batch evaluated row by row group;
+* ``byte_model``   the byte count of one call, from its definition.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 against hand-derived worked examples (``tests/golden/``), closed forms,
 invariants, library special cases and brute force.  The end-to-end numbers are
 not pinned by any value the article prints (it prints no worked example).
 """
-from . import methods, normal_form, indexing, batch  # noqa: F401
+from . import methods, normal_form, indexing, batch, byte_model  # noqa: F401

@@ -1,0 +1,146 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared
+symbol, reports missing devices as an error, and its host byte model equals
+the oracle's restatement bit for bit."""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as WL
+from oracle import byte_model as OBM
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "scute.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import lora_normal_form_gb300 as scute
+    if not os.path.exists(scute.LIB_PATH):
+        from lora_normal_form_gb300 import build as B
+        B.build()
+    return scute
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(scute_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    fns = _declared_functions()
+    for must in ("scute_create", "scute_register_adapter", "scute_linear", "scute_sync_status",
+                 "scute_byte_model", "scute_predict_bytes", "scute_linear_host", "scute_debug_index"):
+        assert must in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll = lib.load()
+    missing = [f for f in _declared_functions() if not hasattr(cdll, f)]
+    assert not missing, missing
+    assert lib.scute_version() == 10000
+
+
+def test_create_without_device_is_an_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(lib.ScuteError) as e:
+        lib.scute_create(0, lib.BF16, 64, 4, 1)
+    assert e.value.code == 9  # SCUTE_ERR_NO_DEVICE
+
+
+def test_create_argument_errors(lib):
+    for args in [(0, 7, 64, 4, 1), (0, 0, 0, 4, 1), (0, 0, 64, 0, 1), (0, 0, 1 << 20, 4, 1)]:
+        with pytest.raises(lib.ScuteError) as e:
+            lib.scute_create(*args)
+        assert e.value.code in (1, 3)
+
+
+def _bm_inputs(w, layer_name, out_dtype):
+    L = w.layer(layer_name)
+    ads = {}
+    for a in w.adapters:
+        ads[a.id] = OBM.adapter_slots_after_fold(a.method, a.slots(layer_name), a.rank)
+    lowrank = any(v["rank"] > 0 for v in ads.values())
+    vera = L.shared_rank > 0 and any(v["vera"] for v in ads.values())
+    return L, ads, lowrank, vera
+
+
+def _c_report(lib, w, L, ads, lowrank, vera, ids, out_dtype, max_adapters):
+    import ctypes
+    arr = (lib.BmAdapter * max_adapters)()
+    for i in range(max_adapters):
+        arr[i].method = -1
+    for aid, v in ads.items():
+        arr[aid].method = lib.METHOD_ID[v["method"]]
+        arr[aid].rank = v["rank"]
+        arr[aid].has_s, arr[aid].has_b, arr[aid].has_R = int(v["s"]), int(v["b"]), int(v["R"])
+        arr[aid].has_vera, arr[aid].has_vera_e = int(v["vera"]), int(v["vera_e"])
+    bl = lib.BmLayer(dtype=lib.FP32 if w.dtype == "fp32" else lib.BF16,
+                     out_dtype=lib.FP32 if out_dtype == "fp32" else lib.BF16,
+                     d_in=L.d_in, d_out=L.d_out, shared_rank=L.shared_rank,
+                     lowrank_launched=int(lowrank), vera_launched=int(vera), max_adapters=max_adapters,
+                     adapters=ctypes.cast(arr, ctypes.POINTER(lib.BmAdapter)))
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    return lib.scute_byte_model(bl, ids, int(ids.size))
+
+
+CASES = [
+    ("tiny_fp32", lambda: WL.tiny_fp32(), "lin", "fp32"),
+    ("decode_small_q", lambda: WL.decode_mixed(n=50, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down")), "q", "bf16"),
+    ("decode_small_up_fp32out", lambda: WL.decode_mixed(n=50, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down")), "up", "fp32"),
+    ("decode_small_nf", lambda: WL.with_nf_adapters(WL.decode_mixed(n=50, shapes=WL.SMALL_PROJ, proj=("q", "down"))), "down", "bf16"),
+    ("decode_llama_k", lambda: WL.decode_mixed(), "k", "bf16"),
+    ("scaling", lambda: WL.scaling_ia3_vera(), "up", "bf16"),
+]
+
+
+@pytest.mark.parametrize("name,make,layer,out_dtype", CASES, ids=[c[0] for c in CASES])
+def test_byte_model_matches_oracle(lib, name, make, layer, out_dtype):
+    w = make()
+    L, ads, lowrank, vera = _bm_inputs(w, layer, out_dtype)
+    A = max(ads) + 3
+    ids = w.ids.copy()
+    if ids.size > 4:
+        ids[1] = -1
+        ids[2] = A - 1   # unregistered id: a base-only token
+    got = _c_report(lib, w, L, ads, lowrank, vera, ids, out_dtype, A)
+    ref = OBM.call_bytes(ids, ads, L.d_in, L.d_out, L.shared_rank, w.dtype, out_dtype, lowrank, vera)
+    assert got["kernels"] == [tuple(k) for k in ref["kernels"]]
+    for k in ("algorithmic_bytes", "adapter_bytes", "base_weight_bytes", "distinct_adapters"):
+        assert got[k] == ref[k], k
+
+
+def test_byte_model_hand_example(lib):
+    """Hand-counted bytes (tests/golden/byte_model_hand.json)."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "byte_model_hand.json")))
+    ads = {int(k): v for k, v in g["adapters"].items()}
+    ref = OBM.call_bytes(g["ids"], ads, g["d_in"], g["d_out"], g["shared_rank"], g["dtype"], g["out_dtype"],
+                         g["lowrank_launched"], g["vera_launched"])
+    exp = g["expected"]
+    assert [list(k) for k in ref["kernels"]] == exp["kernels"]
+    assert ref["algorithmic_bytes"] == exp["algorithmic_bytes"]
+    assert ref["adapter_bytes"] == exp["adapter_bytes"]
+
+    class W:
+        dtype = g["dtype"]
+
+    class Lr:
+        d_in, d_out, shared_rank = g["d_in"], g["d_out"], g["shared_rank"]
+    got = _c_report(lib, W, Lr, ads, g["lowrank_launched"], g["vera_launched"], np.array(g["ids"]),
+                    g["out_dtype"], 8)
+    assert [list(k) for k in got["kernels"]] == exp["kernels"]
+    assert got["algorithmic_bytes"] == exp["algorithmic_bytes"]
+
+
+def test_byte_model_rejects_bad_arguments(lib):
+    import ctypes
+    arr = (lib.BmAdapter * 1)()
+    bl = lib.BmLayer(dtype=0, out_dtype=0, d_in=0, d_out=64, shared_rank=0, lowrank_launched=0,
+                     vera_launched=0, max_adapters=1, adapters=ctypes.cast(arr, ctypes.POINTER(lib.BmAdapter)))
+    with pytest.raises(lib.ScuteError):
+        lib.scute_byte_model(bl, np.zeros(1, np.int32), 1)

@@ -1,0 +1,242 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded inputs.  Indexing is compared bit for bit; floating point is
+graded with the tolerances in ``metrics``."""
+import numpy as np
+import pytest
+
+import workloads as WL
+from oracle import batch as BT
+from oracle import indexing as IX
+import metrics as MX
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def scute(gpu_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return gpu_lib
+
+
+import gpu_harness as H  # noqa: E402
+
+
+# ------------------------------------------------------------------ indexing
+def _index_ctx(scute, A):
+    """A context with adapters of every method registered under ids 0..A-3
+    (ids A-2, A-1 stay free, so they are 'unregistered')."""
+    ctx = scute.Context(dtype="bf16", max_tokens=16384, max_adapters=A, max_layers=1)
+    W = WL.draw_normal(0, "Widx", (64, 64), 0.02, "bf16")
+    ctx.add_layer(0, 64, 64, W)
+    ctx.set_shared(0, 32, WL.draw_normal(0, "Ai", (64, 32), 0.02, "bf16"),
+                   WL.draw_normal(0, "Bi", (32, 64), 0.02, "bf16"))
+    methods = {}
+    order = ["vera", "lora", "oft", "ia3", "dora", "nf"]
+    for i in range(A - 2):
+        m = order[(i * 7 + 3) % 6]
+        t = {"layer": 0}
+        if m == "lora" or m == "dora":
+            t.update(rank=1, c=2.0, A=WL.draw_normal(i, "a", (64, 1), 0.02, "bf16"),
+                     B=WL.draw_normal(i, "b", (1, 64), 0.02, "bf16"))
+            if m == "dora":
+                t["magnitude"] = np.ones(64, np.float32)
+        elif m == "ia3":
+            t["l"] = np.ones(64, np.float32)
+        elif m == "vera":
+            t["d"] = np.ones(32, np.float32)
+        elif m == "oft":
+            t["R"] = WL.draw_cayley_blocks(i, "r", 2, "bf16")
+        else:
+            t["s"] = np.ones(64, np.float32)
+        aid = ctx.register(m, [t])
+        assert aid == i
+        methods[i] = m
+    return ctx, methods
+
+
+@pytest.mark.parametrize("n,A", [(1, 8), (7, 8), (64, 40), (300, 40), (2049, 1024), (8772, 40),
+                                 (16384, 1024)])
+def test_index_bit_exact(scute, n, A):
+    ctx, methods = _index_ctx(scute, A)
+    g = np.random.default_rng(n * 31 + A)
+    ids = g.integers(-1, A, n).astype(np.int32)  # -1 and the unregistered A-2, A-1 included
+    ids_t = torch.from_numpy(ids).cuda()
+    perm = torch.empty(n, dtype=torch.int32, device="cuda")
+    aid = torch.empty(n, dtype=torch.int32, device="cuda")
+    seg_start = torch.full((n + 1,), -7, dtype=torch.int32, device="cuda")
+    seg_aid = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    counts = torch.empty(22, dtype=torch.int32, device="cuda")
+    ctx.debug_index(ids_t, n, perm, aid, seg_start, seg_aid, counts)
+    torch.cuda.synchronize()
+    ref = IX.index_tokens(ids, methods, A)
+    c = counts.cpu().numpy()
+    n_seg = int(c[0])
+    np.testing.assert_array_equal(perm.cpu().numpy(), ref.perm)
+    np.testing.assert_array_equal(aid.cpu().numpy(), ref.aid_sorted)
+    assert n_seg == len(ref.seg_aid)
+    np.testing.assert_array_equal(seg_start.cpu().numpy()[:n_seg + 1], ref.seg_start)
+    np.testing.assert_array_equal(seg_aid.cpu().numpy()[:n_seg], ref.seg_aid)
+    np.testing.assert_array_equal(c[1:8], ref.count)
+    np.testing.assert_array_equal(c[8:15], ref.offset)
+    seg_rank = np.zeros(7, np.int64)
+    for a in ref.seg_aid:
+        seg_rank[IX.METHOD_RANK[methods[int(a)]] if a >= 0 else IX.BASE_RANK] += 1
+    np.testing.assert_array_equal(c[15:22], seg_rank)
+    st = ctx.sync_status()
+    assert st == (5 if ref.bad else 0)
+    ctx.close()
+
+
+# ------------------------------------------------------------------ small shapes, several tiles + ragged tails
+SMALL_NAMES = ("q", "k", "up", "down")
+
+
+def _small_decode(n=50):
+    return WL.with_nf_adapters(WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES))
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_small_decode_parity(scute, out_dtype):
+    w = _small_decode()
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
+    assert ctx.sync_status() == 0
+    for name in SMALL_NAMES:
+        H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_small_prefill_parity(scute, out_dtype):
+    """n > 256: tokens on the 128-row side of the tensor-core tile."""
+    w = WL.with_nf_adapters(WL.prefill_mixed(n_req=6, lo=40, hi=200, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES))
+    assert w.n > 256
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
+    assert ctx.sync_status() == 0
+    for name in SMALL_NAMES:
+        H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
+def test_tiny_fp32(scute):
+    """fp32 single linear, 16 tokens, one adapter per method: max rel <= 1e-4."""
+    w = WL.tiny_fp32()
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, ["lin"], "fp32")
+    assert ctx.sync_status() == 0
+    rep = H.grade(w, "lin", outs["lin"], "fp32")
+    assert rep["fp32_rel"] <= 1e-4
+    ctx.close()
+
+
+@pytest.mark.parametrize("n", [1, 2, 17, 64, 65, 128, 129, 256, 257, 600])
+def test_base_only_equals_xW(scute, n):
+    """All ids -1: every slot is the identity and the output is x W."""
+    w = WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=("q",), n_adapters=5,
+                        ids=np.full(n, -1, np.int32))
+    ctx = H.make_ctx(scute, w, max_tokens=max(n, 64))
+    outs = H.run_layers(ctx, w, ["q"], "fp32")
+    ref = BT.base_output(w, "q")
+    g = H.to_f64(outs["q"])
+    assert MX.fp32_rel_err(g, ref) <= 1e-4
+    ctx.close()
+
+
+@pytest.mark.parametrize("method", ["lora", "dora", "ia3", "vera", "oft"])
+def test_single_adapter_batch(scute, method):
+    """Every token on one adapter (one segment), plus a one-token call."""
+    k = WL.MOD5.index(method)
+    n = 40
+    w = WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES, n_adapters=5,
+                        ids=np.full(n, k, np.int32))
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, SMALL_NAMES, "fp32")
+    for name in SMALL_NAMES:
+        H.grade(w, name, outs[name], "fp32")
+    w1 = WL.decode_mixed(n=1, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES, n_adapters=5,
+                         ids=np.full(1, k, np.int32))
+    ctx1 = H.make_ctx(scute, w1)
+    outs1 = H.run_layers(ctx1, w1, SMALL_NAMES, "fp32")
+    for name in SMALL_NAMES:
+        H.grade(w1, name, outs1[name], "fp32")
+    ctx.close()
+    ctx1.close()
+
+
+def test_rank1_and_rank64(scute):
+    n = 48
+    for rank in (1, 64):
+        w = WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=("q", "down"), n_adapters=4, rank=rank,
+                            ids=np.random.default_rng(rank).integers(-1, 4, n).astype(np.int32))
+        ctx = H.make_ctx(scute, w)
+        outs = H.run_layers(ctx, w, ("q", "down"), "fp32")
+        for name in ("q", "down"):
+            H.grade(w, name, outs[name], "fp32")
+        ctx.close()
+
+
+def test_bad_ids_become_base_and_are_reported(scute):
+    w = _small_decode(n=32)
+    ids = w.ids.copy()
+    ids[3] = 999
+    ids[7] = -5
+    ctx = H.make_ctx(scute, w, max_adapters=1024)
+    outs = H.run_layers(ctx, w, ["q"], "fp32", ids=ids)
+    assert ctx.sync_status() == 5  # SCUTE_ERR_BAD_ADAPTER
+    assert ctx.sync_status() == 0  # cleared by the read
+    ref = BT.base_output(w, "q", rows=[3, 7])
+    g = H.to_f64(outs["q"][[3, 7]])
+    assert MX.fp32_rel_err(g, ref) <= 1e-4
+    ctx.close()
+
+
+def test_n_zero_is_a_no_op(scute):
+    w = _small_decode(n=8)
+    ctx = H.make_ctx(scute, w)
+    before = ctx.launch_count()
+    out = torch.empty(0, 1056, device="cuda", dtype=torch.bfloat16)
+    x = torch.empty(0, 544, device="cuda", dtype=torch.bfloat16)
+    ids = torch.empty(0, device="cuda", dtype=torch.int32)
+    ctx.linear(x, ids, ctx.layer_ids["q"], out, "bf16", n=0)
+    assert ctx.launch_count() == before
+    ctx.close()
+
+
+def test_linear_host_matches_linear(scute):
+    w = _small_decode(n=24)
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, ["up"], "bf16")
+    L = w.layer("up")
+    x_host = torch.from_numpy(L.get("x").view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_host = torch.from_numpy(w.ids.copy()).pin_memory()
+    out_host = torch.empty(w.n, L.d_out, dtype=torch.bfloat16).pin_memory()
+    ctx.linear_host(x_host, ids_host, ctx.layer_ids["up"], out_host, "bf16",
+                    stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, outs["up"].cpu())
+    ctx.close()
+
+
+def test_cuda_graph_replay_matches_eager(scute):
+    w = _small_decode(n=40)
+    ctx = H.make_ctx(scute, w)
+    eager = H.run_layers(ctx, w, SMALL_NAMES, "bf16")
+    ids_t = torch.from_numpy(w.ids.copy()).cuda()
+    xs = {n: H.dev(w.layer(n).get("x")) for n in SMALL_NAMES}
+    outs = {n: torch.zeros(w.n, w.layer(n).d_out, device="cuda", dtype=torch.bfloat16) for n in SMALL_NAMES}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for n in SMALL_NAMES:
+                ctx.linear(xs[n], ids_t, ctx.layer_ids[n], outs[n], "bf16", stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for n in SMALL_NAMES:
+        assert torch.equal(outs[n], eager[n]), n
+    ctx.close()
