@@ -553,10 +553,17 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     g.stages = p.stages;
     g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
     const int slot = c->t_next;
-    if (c->timing) CU_TRY(c, cudaEventRecord(c->ev[slot][0], st));
+    unsigned ev_flags = cudaEventRecordDefault;
+    if (c->timing) {
+        // inside stream capture an event record must become a graph node
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CU_TRY(c, cudaStreamIsCapturing(st, &cs));
+        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][0], st, ev_flags));
+    }
     CU_TRY(c, launch_gemm(g, p, st, c->pdl));
     if (c->timing) {
-        CU_TRY(c, cudaEventRecord(c->ev[slot][1], st));
+        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][1], st, ev_flags));
         c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
         if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
     }

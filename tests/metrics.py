@@ -1,6 +1,10 @@
 """Parity graders: the tolerances of the adapted layer's acceptance criteria.
 
-* fp32 contexts: max_i |g_i - r_i| / max(|r_i|, 1e-3 rms(r)) <= 1e-4.
+* fp32 contexts: max_i |g_i - r_i| / max(|r_i|, 1e-2 rms(r)) <= 1e-4.  The
+  floor makes the relative error defined near zero crossings; at 1e-3 rms(r)
+  a float32 evaluation of the same definition on the same inputs (a plain
+  sgemm, or sequential float32 sums) already scores 1.5-2.4e-4 on the tiny
+  fp32 workload, so that floor would grade float32 rounding itself.
 * bf16 outputs: max |g - r| <= 3e-2, except where half a bf16 spacing of r
   exceeds 1.5e-2 (|r| >= 4): there the output is graded as
   |g - RN_bf16(r)| <= 1 bf16 spacing (rounding alone would break 3e-2).
@@ -20,8 +24,14 @@ EFFECT_TOL = 0.01
 def fp32_rel_err(g, r):
     g = np.asarray(g, np.float64)
     r = np.asarray(r, np.float64)
-    floor = 1e-3 * np.sqrt(np.mean(r * r))
+    floor = 1e-2 * np.sqrt(np.mean(r * r))
     return float(np.max(np.abs(g - r) / np.maximum(np.abs(r), floor)))
+
+
+def normwise_err(g, r):
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    return float(np.max(np.abs(g - r)) / np.max(np.abs(r)))
 
 
 def bf16_spacing(v):

@@ -134,14 +134,15 @@ def test_tiny_fp32(scute):
 
 @pytest.mark.parametrize("n", [1, 2, 17, 64, 65, 128, 129, 256, 257, 600])
 def test_base_only_equals_xW(scute, n):
-    """All ids -1: every slot is the identity and the output is x W."""
+    """All ids -1: every slot is the identity and the output is x W (bf16
+    inputs, float32 accumulation: normwise error at the float32 level)."""
     w = WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=("q",), n_adapters=5,
                         ids=np.full(n, -1, np.int32))
     ctx = H.make_ctx(scute, w, max_tokens=max(n, 64))
     outs = H.run_layers(ctx, w, ["q"], "fp32")
     ref = BT.base_output(w, "q")
     g = H.to_f64(outs["q"])
-    assert MX.fp32_rel_err(g, ref) <= 1e-4
+    assert MX.normwise_err(g, ref) <= 1e-5
     ctx.close()
 
 
@@ -189,7 +190,7 @@ def test_bad_ids_become_base_and_are_reported(scute):
     assert ctx.sync_status() == 0  # cleared by the read
     ref = BT.base_output(w, "q", rows=[3, 7])
     g = H.to_f64(outs["q"][[3, 7]])
-    assert MX.fp32_rel_err(g, ref) <= 1e-4
+    assert MX.normwise_err(g, ref) <= 1e-5
     ctx.close()
 
 
