@@ -523,14 +523,53 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     const int out_f32 = out_dtype == SCUTE_FP32 ? 1 : 0;
     int k = 0;
 
-    // 1. token indexing
-    CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
-                           c->d_seg_aid, c->d_meta, c->d_status, st));
-    ++k;
-    // 2. rotation prologue into the sorted token operand
-    CU_TRY(c, launch_gather_rotate(f32, x, L.d_in, nn, c->d_perm, c->d_aid, slots, c->xs, L.kdim, st, c->pdl));
-    ++k;
-    // 3. base GEMM with the s / b epilogue
+    const int lr_rmax = L.n_lr > 0 ? max_owned_rank(c, layer) : 0;
+    const bool vera_on = L.rv > 0 && L.n_vera > 0;
+    // Decode batches (bf16, n <= 128): one prologue launch (indexing, rotation,
+    // both shrinks) and one GEMM whose epilogue applies s, b, the owned
+    // low-rank expand and the VeRA expand (as extra tcgen05 K blocks).
+    const bool fused = !f32 && nn <= 128;
+    if (fused) {
+        PrepArgs pa;
+        memset(&pa, 0, sizeof(pa));
+        pa.x = x;
+        pa.d_in = L.d_in;
+        pa.n = nn;
+        pa.kdim = L.kdim;
+        pa.ids = ids;
+        pa.method_tab = c->d_method;
+        pa.A = c->max_adapters;
+        pa.slots = slots;
+        pa.perm = c->d_perm;
+        pa.aid_s = c->d_aid;
+        pa.seg_start = c->d_seg_start;
+        pa.seg_aid = c->d_seg_aid;
+        pa.meta = c->d_meta;
+        pa.status = c->d_status;
+        pa.xs = c->xs;
+        pa.v = c->v_part;
+        pa.v_ld = MAX_RANK;
+        pa.U = c->U;
+        pa.u_ld = L.krv;
+        pa.Ash = L.Ash;
+        pa.rv = vera_on ? L.rv : 0;
+        pa.n_rot = (L.d_in + 255) / 256;
+        pa.lr_groups = lr_rmax > 0 ? (lr_rmax + 3) / 4 : 1;
+        pa.n_lr = lr_rmax > 0 ? (nn < L.n_lr ? nn : L.n_lr) * pa.lr_groups : 0;
+        pa.n_vera = vera_on ? (L.rv + 3) / 4 : 0;
+        CU_TRY(c, launch_prep(pa, pa.n_rot + pa.n_lr + pa.n_vera, st, c->pdl));
+        ++k;
+    } else {
+        // 1. token indexing
+        CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
+                               c->d_seg_aid, c->d_meta, c->d_status, st));
+        ++k;
+        // 2. rotation prologue into the sorted token operand
+        CU_TRY(c, launch_gather_rotate(f32, x, L.d_in, nn, c->d_perm, c->d_aid, slots, c->xs, L.kdim, st,
+                                       c->pdl));
+        ++k;
+    }
+    // 3. base GEMM with the s / b epilogue (and the fused terms)
     const bool tok_on_p = nn > 256;
     GemmArgs g;
     memset(&g, 0, sizeof(g));
@@ -548,10 +587,25 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     g.aid_s = c->d_aid;
     g.out = out;
     g.status = c->d_status;
-    GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms);
+    if (fused) {
+        if (lr_rmax > 0) {
+            g.v = c->v_part;
+            g.v_ld = MAX_RANK;
+            g.lr_rmax = lr_rmax;
+        }
+        if (vera_on) {
+            g.mapVP = L.mapBsh;
+            g.mapVQ = L.mapU;
+            g.vera_kb = (L.krv * c->esz + 127) / 128;
+        }
+    }
+    GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms, g.lr_rmax);
     g.splits = p.splits;
     g.stages = p.stages;
     g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
+    if (!tok_on_p &&
+        (size_t)p.stages * (128 * 128 + p.bn * 128) < (size_t)(g.vera_kb ? 2 : 1) * p.bn * 128 * 4)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "split-K partial tiles do not fit the pipeline buffers");
     const int slot = c->t_next;
     unsigned ev_flags = cudaEventRecordDefault;
     if (c->timing) {
@@ -569,18 +623,18 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     }
     ++k;
     // 4. owned low-rank shrink / expand
-    if (L.n_lr > 0) {
+    if (L.n_lr > 0 && !fused) {
         int bound = nn;
         int reg = 0;
         for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
         if (reg + 1 < bound) bound = reg + 1;
         CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, nn, bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
                                  c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
-                                 max_owned_rank(c, layer)));
+                                 lr_rmax));
         k += 2;
     }
     // 5. VeRA: shared shrink then shared expand over the VeRA rows only
-    if (L.rv > 0 && L.n_vera > 0) {
+    if (vera_on && !fused) {
         GemmArgs v;
         memset(&v, 0, sizeof(v));
         v.mapP = tok_on_p ? L.mapXs : L.mapAsh;

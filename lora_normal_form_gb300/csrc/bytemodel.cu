@@ -77,22 +77,40 @@ scute_status scute_byte_model(const scute_bm_layer *L, const int32_t *ids, int64
     }
     const int64_t segs = distinct + (has_base ? 1 : 0);
 
-    add_kernel(rep, "index", 4 * n + 8 * n + 4 * (segs + 1) + 4 * segs + 88, 0);
-    add_kernel(rep, "rotate", n * din * E + 8 * n + sum_R + n * kd * E, 2 * n_rot * din * 32);
-    add_kernel(rep, "base_gemm", dout * kd * E + n * kd * E + sum_sb + 8 * n + n * dout * Eo,
-               2 * n * kd * dout);
-    if (L->lowrank_launched) {
-        const int64_t ks = scute::lowrank_ks(L->d_in, nullptr);
-        add_kernel(rep, "lr_shrink", n_lr * din * E + sum_A + ks * lr_rank_rows * 4, 2 * lr_rank_rows * din);
-        add_kernel(rep, "lr_expand", ks * lr_rank_rows * 4 + sum_B + 2 * n_lr * dout * Eo,
-                   2 * lr_rank_rows * dout);
-    }
-    if (L->vera_launched) {
-        const int64_t shA = n_v > 0 ? rv * kd * E : 0;
-        const int64_t shB = n_v > 0 ? dout * krv * E : 0;
-        add_kernel(rep, "vera_shrink", n_v * kd * E + shA + sum_d + n_v * krv * E, 2 * n_v * rv * kd);
-        add_kernel(rep, "vera_expand", n_v * krv * E + shB + sum_e + 2 * n_v * dout * Eo,
-                   2 * n_v * krv * dout);
+    // bf16 calls with at most 128 tokens run the fused decode plan: one
+    // prologue (indexing, rotation, both shrinks) and one GEMM whose epilogue
+    // applies s, b and both expands
+    const bool fused = !f32 && n <= 128;
+    const int64_t index_out = 8 * n + 4 * (segs + 1) + 4 * segs + 88;
+    if (fused) {
+        const int64_t shA = n_v > 0 ? rv * din * E : 0;
+        const int64_t shB = n_v > 0 ? dout * rv * E : 0;
+        add_kernel(rep, "prep",
+                   4 * n + n * din * E + sum_R + sum_A + shA + sum_d + n * kd * E + lr_rank_rows * 4 +
+                       n_v * rv * E + index_out,
+                   2 * n_rot * din * 32 + 2 * lr_rank_rows * din + 2 * n_v * rv * din);
+        add_kernel(rep, "base_gemm",
+                   dout * kd * E + n * kd * E + sum_sb + sum_B + lr_rank_rows * 4 + shB + n_v * rv * E + sum_e +
+                       8 * n + n * dout * Eo,
+                   2 * n * kd * dout + 2 * lr_rank_rows * dout + 2 * n_v * rv * dout);
+    } else {
+        add_kernel(rep, "index", 4 * n + index_out, 0);
+        add_kernel(rep, "rotate", n * din * E + 8 * n + sum_R + n * kd * E, 2 * n_rot * din * 32);
+        add_kernel(rep, "base_gemm", dout * kd * E + n * kd * E + sum_sb + 8 * n + n * dout * Eo,
+                   2 * n * kd * dout);
+        if (L->lowrank_launched) {
+            const int64_t ks = scute::lowrank_ks(L->d_in, nullptr);
+            add_kernel(rep, "lr_shrink", n_lr * din * E + sum_A + ks * lr_rank_rows * 4, 2 * lr_rank_rows * din);
+            add_kernel(rep, "lr_expand", ks * lr_rank_rows * 4 + sum_B + 2 * n_lr * dout * Eo,
+                       2 * lr_rank_rows * dout);
+        }
+        if (L->vera_launched) {
+            const int64_t shA = n_v > 0 ? rv * kd * E : 0;
+            const int64_t shB = n_v > 0 ? dout * krv * E : 0;
+            add_kernel(rep, "vera_shrink", n_v * kd * E + shA + sum_d + n_v * krv * E, 2 * n_v * rv * kd);
+            add_kernel(rep, "vera_expand", n_v * krv * E + shB + sum_e + 2 * n_v * dout * Eo,
+                       2 * n_v * krv * dout);
+        }
     }
     const int64_t shared = n_v > 0 ? (din + dout) * rv * E : 0;
     rep->base_weight_bytes = din * dout * E;

@@ -54,6 +54,8 @@ enum : int { EPI_BASE = 0, EPI_VERA_D = 1, EPI_VERA_E = 2 };
 struct GemmArgs {
     CUtensorMap mapP;          // P operand: 128-row tiles
     CUtensorMap mapQ;          // Q operand: BN-row tiles
+    CUtensorMap mapVP;         // fused VeRA expand: P = B_sh^T [d_out][rv]
+    CUtensorMap mapVQ;         // fused VeRA expand: Q = U [tokens][rv] (sorted rows)
     int kblocks;               // K extent in 128-byte blocks
     int n_ft;                  // tiles along the feature dimension
     int n_feat;                // features (d_out, or the shared rank)
@@ -76,6 +78,11 @@ struct GemmArgs {
     void *out;                 // [n, ld_out]
     void *U;                   // VeRA intermediate
     int *status;
+    // fused epilogue (features-on-P orientation only)
+    int vera_kb;               // VeRA expand K blocks folded into this GEMM (0 = none)
+    const float *v;            // owned low-rank intermediate [tokens][v_ld] (null = none)
+    int v_ld;
+    int lr_rmax;               // largest owned rank on the layer (v columns preloaded)
 };
 
 struct GemmPlan {
@@ -87,7 +94,8 @@ struct GemmPlan {
     size_t smem;
 };
 
-GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms);
+GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms,
+                   int lr_rmax = 0);
 cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl);
 
 // K splits of the owned low-rank shrink: at most KS_MAX chunks of a multiple
@@ -116,6 +124,31 @@ cudaError_t allow_max_dynamic_smem(K kernel) {
                                  optin - (int)fa.sharedSizeBytes);
     return e;
 }
+
+// ---------------------------------------------------------------- decode prologue
+constexpr int PREP_MAX_TOKENS = 256;
+
+struct PrepArgs {
+    const void *x;             // [n, d_in] bf16, token order
+    int d_in, n, kdim;
+    const int32_t *ids;
+    const int8_t *method_tab;
+    int A;                     // max adapters
+    const Slot *slots;         // this layer's slot row
+    int *perm, *aid_s, *seg_start, *seg_aid;
+    IndexMeta *meta;
+    int *status;
+    void *xs;                  // [max_tokens, kdim] sorted, rotated token operand
+    float *v;                  // [max_tokens, v_ld] owned low-rank intermediate
+    int v_ld;
+    void *U;                   // [max_tokens, u_ld] bf16 VeRA intermediate (d applied)
+    int u_ld;
+    const void *Ash;           // [rv, d_in] shared VeRA A, K-major
+    int rv;
+    int n_rot, n_lr, lr_groups, n_vera;   // work items per kind (grid = their sum)
+};
+size_t prep_smem_bytes();
+cudaError_t launch_prep(const PrepArgs &p, int grid, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- other kernels
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,

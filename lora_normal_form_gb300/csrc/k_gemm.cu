@@ -103,65 +103,54 @@ __device__ __forceinline__ void store_elem(void *out, int f32, size_t idx, float
     }
 }
 
-// Per-row context of the epilogue: which output row and which live vectors.
-struct RowCtx {
+// Per-token context of the epilogue: which output row and which live slots.
+struct TokMeta {
     long long out_row;     // token index (output row) or U row
     const float *v1;       // s (BASE), d (VERA_D), e (VERA_E)
     const float *v2;       // b (BASE)
+    const void *B;         // fused owned B' [rank][n_feat] (BASE)
+    const float *ve;       // fused VeRA e (BASE)
+    int rank;              // fused owned rank
+    int vera;              // fused: the row is a VeRA row
 };
 
-__device__ __forceinline__ RowCtx row_ctx(const GemmArgs &g, int i, int sorted_base) {
-    RowCtx r;
+__device__ __forceinline__ TokMeta tok_meta(const GemmArgs &g, int i, int sorted_base) {
+    TokMeta m;
     const int srow = sorted_base + i;
     const int a = g.aid_s[srow];
-    r.v1 = nullptr;
-    r.v2 = nullptr;
+    m.v1 = nullptr;
+    m.v2 = nullptr;
+    m.B = nullptr;
+    m.ve = nullptr;
+    m.rank = 0;
+    m.vera = 0;
     if (g.epi == EPI_VERA_D) {
-        r.out_row = i;
-        if (a >= 0) r.v1 = g.slots[a].vd;
-    } else {
-        r.out_row = g.perm[srow];
-        if (a >= 0) {
-            if (g.epi == EPI_BASE) {
-                r.v1 = g.slots[a].s;
-                r.v2 = g.slots[a].b;
-            } else {
-                r.v1 = g.slots[a].ve;
-            }
-        }
+        m.out_row = i;
+        if (a >= 0) m.v1 = g.slots[a].vd;
+        return m;
     }
-    return r;
+    m.out_row = g.perm[srow];
+    if (a < 0) return m;
+    const Slot &sl = g.slots[a];
+    if (g.epi == EPI_VERA_E) {
+        m.v1 = sl.ve;
+        return m;
+    }
+    m.v1 = sl.s;
+    m.v2 = sl.b;
+    if (g.v && sl.B && sl.rank > 0) {
+        m.B = sl.B;
+        m.rank = sl.rank;
+    }
+    if (g.vera_kb && sl.vd) {
+        m.vera = 1;
+        m.ve = sl.ve;
+    }
+    return m;
 }
 
-// One output element.
-__device__ __forceinline__ void emit1(const GemmArgs &g, const RowCtx &r, int j, float acc) {
-    if (g.epi == EPI_BASE) {
-        float v = acc;
-        if (r.v1) v *= __ldg(r.v1 + j);
-        if (r.v2) v += __ldg(r.v2 + j);
-        store_elem(g.out, g.out_f32, (size_t)r.out_row * g.ld_out + j, v, false);
-    } else if (g.epi == EPI_VERA_E) {
-        float v = acc;
-        if (r.v1) v *= __ldg(r.v1 + j);
-        store_elem(g.out, g.out_f32, (size_t)r.out_row * g.ld_out + j, v, true);
-    } else {
-        float v = r.v1 ? acc * __ldg(r.v1 + j) : 0.f;
-        if (g.u_split3) {
-            float *U = reinterpret_cast<float *>(g.U) + (size_t)r.out_row * g.ldu;
-            const float hi = ptx::to_tf32(v);
-            U[j] = hi;
-            U[g.u_rank + j] = hi;
-            U[2 * g.u_rank + j] = v - hi;
-        } else {
-            reinterpret_cast<__nv_bfloat16 *>(g.U)[(size_t)r.out_row * g.ldu + j] =
-                __float2bfloat16_rn(v);
-        }
-    }
-}
-
-// 32 consecutive features [j0, j0+32) of one row (normal orientation).
-__device__ __forceinline__ void emit32(const GemmArgs &g, const RowCtx &r, int j0,
-                                       const float (&acc)[32]) {
+// 32 consecutive features [j0, j0+32) of one row (tokens-on-P orientation).
+__device__ __forceinline__ void emit32(const GemmArgs &g, const TokMeta &r, int j0, const float (&acc)[32]) {
     float v[32];
     if (g.epi == EPI_VERA_D) {
 #pragma unroll
@@ -240,6 +229,147 @@ __device__ __forceinline__ void emit32(const GemmArgs &g, const RowCtx &r, int j
     }
 }
 
+// Eight consecutive features [j0, j0+8) of token m (features-on-P orientation):
+// base / VeRA accumulators in, slots applied, eight outputs stored with one
+// vector store.  All loads of one item are independent 16-byte loads.
+__device__ __forceinline__ void emit8(const GemmArgs &g, const TokMeta &m, const float *vrow, int j0,
+                                      const float (&acc)[8], const float (&vacc)[8]) {
+    float y[8];
+    if (g.epi == EPI_VERA_D) {
+        if (m.v1) {
+            const float4 d0 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0));
+            const float4 d1 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0 + 4));
+            y[0] = acc[0] * d0.x; y[1] = acc[1] * d0.y; y[2] = acc[2] * d0.z; y[3] = acc[3] * d0.w;
+            y[4] = acc[4] * d1.x; y[5] = acc[5] * d1.y; y[6] = acc[6] * d1.z; y[7] = acc[7] * d1.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[k] = 0.f;
+        }
+        if (g.u_split3) {
+            float *U = reinterpret_cast<float *>(g.U) + (size_t)m.out_row * g.ldu + j0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float hi = ptx::to_tf32(y[k]);
+                U[k] = hi;
+                U[g.u_rank + k] = hi;
+                U[2 * g.u_rank + k] = y[k] - hi;
+            }
+        } else {
+            uint4 pk;
+            __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(g.U) + (size_t)m.out_row * g.ldu + j0) = pk;
+        }
+        return;
+    }
+    if (g.epi == EPI_BASE) {
+        float s8[8], b8[8];
+        if (m.v1) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0));
+            const float4 a1 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0 + 4));
+            s8[0] = a0.x; s8[1] = a0.y; s8[2] = a0.z; s8[3] = a0.w; s8[4] = a1.x; s8[5] = a1.y; s8[6] = a1.z; s8[7] = a1.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s8[k] = 1.f;
+        }
+        if (m.v2) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4 *>(m.v2 + j0));
+            const float4 a1 = __ldg(reinterpret_cast<const float4 *>(m.v2 + j0 + 4));
+            b8[0] = a0.x; b8[1] = a0.y; b8[2] = a0.z; b8[3] = a0.w; b8[4] = a1.x; b8[5] = a1.y; b8[6] = a1.z; b8[7] = a1.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) b8[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = acc[k] * s8[k] + b8[k];
+        if (m.B) {
+            // owned low-rank expand: y += v_t B'[:, j0:j0+8], 16 ranks per batch of loads
+            const __nv_bfloat16 *B = reinterpret_cast<const __nv_bfloat16 *>(m.B) + j0;
+            for (int q0 = 0; q0 < m.rank; q0 += 16) {
+                uint4 bq[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(B + (size_t)(q0 + q) * g.n_feat));
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    if (q0 + q < m.rank) {
+                        const float vq = vrow[q0 + q];
+                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&bq[q]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(h[e]);
+                            y[2 * e] = fmaf(vq, f.x, y[2 * e]);
+                            y[2 * e + 1] = fmaf(vq, f.y, y[2 * e + 1]);
+                        }
+                    }
+                }
+            }
+        }
+        if (m.vera) {
+            if (m.ve) {
+                const float4 a0 = __ldg(reinterpret_cast<const float4 *>(m.ve + j0));
+                const float4 a1 = __ldg(reinterpret_cast<const float4 *>(m.ve + j0 + 4));
+                y[0] += vacc[0] * a0.x; y[1] += vacc[1] * a0.y; y[2] += vacc[2] * a0.z; y[3] += vacc[3] * a0.w;
+                y[4] += vacc[4] * a1.x; y[5] += vacc[5] * a1.y; y[6] += vacc[6] * a1.z; y[7] += vacc[7] * a1.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[k] += vacc[k];
+            }
+        }
+    } else {  // EPI_VERA_E: out += acc * e
+        if (m.v1) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0));
+            const float4 a1 = __ldg(reinterpret_cast<const float4 *>(m.v1 + j0 + 4));
+            y[0] = acc[0] * a0.x; y[1] = acc[1] * a0.y; y[2] = acc[2] * a0.z; y[3] = acc[3] * a0.w;
+            y[4] = acc[4] * a1.x; y[5] = acc[5] * a1.y; y[6] = acc[6] * a1.z; y[7] = acc[7] * a1.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[k] = acc[k];
+        }
+    }
+    const bool add = g.epi == EPI_VERA_E;
+    if (g.out_f32) {
+        float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(g.out) + (size_t)m.out_row * g.ld_out + j0);
+        float4 w0 = make_float4(y[0], y[1], y[2], y[3]), w1 = make_float4(y[4], y[5], y[6], y[7]);
+        if (add) {
+            const float4 p0 = o[0], p1 = o[1];
+            w0.x += p0.x; w0.y += p0.y; w0.z += p0.z; w0.w += p0.w;
+            w1.x += p1.x; w1.y += p1.y; w1.z += p1.z; w1.w += p1.w;
+        }
+        o[0] = w0;
+        o[1] = w1;
+    } else {
+        uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(g.out) + (size_t)m.out_row * g.ld_out + j0);
+        if (add) {
+            const uint4 prev = *o;
+            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&prev);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(q2[e]);
+                y[2 * e] += f.x;
+                y[2 * e + 1] += f.y;
+            }
+        }
+        uint4 pk;
+        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+        *o = pk;
+    }
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 template <int BN, bool TF32>
 __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ GemmArgs g) {
@@ -253,6 +383,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                                                 ~static_cast<uintptr_t>(1023));
     const int stages = g.stages;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + stages * STAGE_BYTES);
+    TokMeta *tmeta = reinterpret_cast<TokMeta *>(reinterpret_cast<uint8_t *>(ctrl) + CTRL_BYTES);
+    float *vtile = reinterpret_cast<float *>(tmeta + BN);
     volatile int *abort_flag = &ctrl->abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,6 +405,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     if (tile0 >= n_tiles) return;  // uniform across a cluster
     const int kb0 = (int)((long long)crank * g.kblocks / splits);
     const int kb1 = (int)((long long)(crank + 1) * g.kblocks / splits);
+    // fused VeRA expand K blocks of this CTA: j = crank, crank + splits, ...
+    const bool my_vera = g.vera_kb > crank;
+    const int n_vera_ranks = g.vera_kb < splits ? g.vera_kb : splits;
 
     // ---- set-up
     if (threadIdx.x == 0) {
@@ -289,6 +424,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&g.mapP);
         ptx::prefetch_tmap(&g.mapQ);
+        if (g.vera_kb) {
+            ptx::prefetch_tmap(&g.mapVP);
+            ptx::prefetch_tmap(&g.mapVQ);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&ctrl->tmem_base), NCOLS);
@@ -310,29 +449,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                 const int ft = tile % g.n_ft, tt = tile / g.n_ft;
                 const int prow = g.tok_on_p ? tok_base + tt * TILE_M : ft * TILE_M;
                 const int qrow = g.tok_on_p ? ft * BN : tok_base + tt * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const int nkb = (kb1 - kb0) + (my_vera ? (g.vera_kb - crank + splits - 1) / splits : 0);
+                for (int it = 0; it < nkb; ++it) {
+                    const bool vblk = it >= kb1 - kb0;
+                    const int kc = vblk ? (crank + (it - (kb1 - kb0)) * splits) * KE : (kb0 + it) * KE;
+                    const CUtensorMap *mP = vblk ? &g.mapVP : &g.mapP;
+                    const CUtensorMap *mQ = vblk ? &g.mapVQ : &g.mapQ;
                     if (!wait_bar(ptx::smem_u32(&ctrl->empty[stage]), phase ^ 1, abort_flag)) goto prod_done;
                     const uint32_t fb = ptx::smem_u32(&ctrl->full[stage]);
                     const uint32_t sP = ptx::smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sQ = sP + TILE_M * 128;
-                    const int kc = kb * KE;
                     ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     if (!g.tok_on_p) {
                         // P (weights) does not depend on earlier kernels: it is
                         // fetched before the grid dependency resolves.
-                        ptx::tma_load_2d(sP, &g.mapP, kc, prow, fb);
-                        ptx::tma_load_2d(sP + BOX_BYTES, &g.mapP, kc, prow + BOX_ROWS, fb);
+                        ptx::tma_load_2d(sP, mP, kc, prow, fb);
+                        ptx::tma_load_2d(sP + BOX_BYTES, mP, kc, prow + BOX_ROWS, fb);
                         if (!dep_done) { ptx::grid_dep_wait(); dep_done = true; }
 #pragma unroll
                         for (int j = 0; j < BN / BOX_ROWS; ++j)
-                            ptx::tma_load_2d(sQ + j * BOX_BYTES, &g.mapQ, kc, qrow + j * BOX_ROWS, fb);
+                            ptx::tma_load_2d(sQ + j * BOX_BYTES, mQ, kc, qrow + j * BOX_ROWS, fb);
                     } else {
                         if (!dep_done) { ptx::grid_dep_wait(); dep_done = true; }
-                        ptx::tma_load_2d(sP, &g.mapP, kc, prow, fb);
-                        ptx::tma_load_2d(sP + BOX_BYTES, &g.mapP, kc, prow + BOX_ROWS, fb);
+                        ptx::tma_load_2d(sP, mP, kc, prow, fb);
+                        ptx::tma_load_2d(sP + BOX_BYTES, mP, kc, prow + BOX_ROWS, fb);
 #pragma unroll
                         for (int j = 0; j < BN / BOX_ROWS; ++j)
-                            ptx::tma_load_2d(sQ + j * BOX_BYTES, &g.mapQ, kc, qrow + j * BOX_ROWS, fb);
+                            ptx::tma_load_2d(sQ + j * BOX_BYTES, mQ, kc, qrow + j * BOX_ROWS, fb);
                     }
                     ++issued;
                     if (++stage == stages) { stage = 0; phase ^= 1; }
@@ -360,8 +503,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             for (int tile = tile0; tile < n_tiles; tile += tstep) {
                 if (!wait_bar(ptx::smem_u32(&ctrl->tempty[acc]), acc_phase ^ 1, abort_flag)) goto mma_done;
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const int nb = kb1 - kb0;
+                const int nkb = nb + (my_vera ? (g.vera_kb - crank + splits - 1) / splits : 0);
+                for (int it = 0; it < nkb; ++it) {
+                    const bool vblk = it >= nb;
+                    // the fused VeRA product accumulates into the second buffer
+                    const uint32_t d_tmem = tmem_base + (uint32_t)((vblk ? 1 : acc) * BN);
+                    const bool first = vblk ? (it == nb) : (it == 0);
                     if (!wait_bar(ptx::smem_u32(&ctrl->full[stage]), phase, abort_flag)) goto mma_done;
                     ptx::tc_fence_after();
                     const uint32_t sP = ptx::smem_u32(smem + stage * STAGE_BYTES);
@@ -369,7 +517,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                     const uint64_t db = sw128_desc(sP + TILE_M * 128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
                         if (TF32)
                             ptx::mma_tf32(d_tmem, da + 2 * kk, db + 2 * kk, IDESC, accum);
                         else
@@ -390,8 +538,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     } else {
         // ================================================= epilogue warps
         ptx::grid_dep_wait();
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int et = threadIdx.x - 64;   // 0..127
+        const int q = warp & 3;            // TMEM lane quadrant this warp may access
         const int row = q * 32 + lane;
+        if (!g.tok_on_p) {
+            // one token tile (n_tok <= BN): per-token metadata and the owned
+            // low-rank intermediate go to shared memory while the K loop runs
+            for (int t = et; t < BN; t += 128)
+                if (t < n_tok) tmeta[t] = tok_meta(g, t, sorted_base);
+            if (g.v) {
+                const int R = g.lr_rmax;
+                for (int e = et; e < BN * R; e += 128) {
+                    const int t = e / R, c = e - t * R;
+                    vtile[e] = t < n_tok ? g.v[(size_t)(sorted_base + t) * g.v_ld + c] : 0.f;
+                }
+            }
+            epi_bar();
+        }
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = tile0; tile < n_tiles; tile += tstep) {
@@ -399,46 +562,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             ptx::tc_fence_after();
             const int ft = tile % g.n_ft, tt = tile / g.n_ft;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (splits > 1) {
-                // partial tile -> own shared memory, [token][128 features]
+            const uint32_t tbv = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)BN;
+            if (!g.tok_on_p) {
+                // features on rows, tokens on columns: the (partial) tile goes to
+                // this CTA's shared memory as [token][128 features]; the
+                // reduction and the epilogue run after the block-wide barrier
                 float *red = reinterpret_cast<float *>(smem);
+                float *redv = red + BN * TILE_M;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     ptx::tmem_ld32(tb + c * 32, v);
 #pragma unroll
                     for (int k = 0; k < 32; ++k) red[(c * 32 + k) * TILE_M + row] = v[k];
-                }
-            } else if (!g.tok_on_p) {
-                // features on rows, tokens on columns
-                const int j = ft * TILE_M + row;
-                int last_i = -1;
-                RowCtx rc;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    ptx::tmem_ld32(tb + c * 32, v);
-                    if (c == BN / 32 - 1) {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[acc]));
-                    }
-                    if (j < g.n_feat) {
-#pragma unroll 1
-                        for (int k = 0; k < 32; ++k) {
-                            const int i = tt * BN + c * 32 + k;
-                            if (i >= n_tok) break;
-                            if (i != last_i) { rc = row_ctx(g, i, sorted_base); last_i = i; }
-                            emit1(g, rc, j, v[k]);
-                        }
+                    if (my_vera) {
+                        ptx::tmem_ld32(tbv + c * 32, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) redv[(c * 32 + k) * TILE_M + row] = v[k];
                     }
                 }
             } else {
                 // tokens on rows, features on columns
                 const int i = tt * TILE_M + row;
                 const bool live = i < n_tok;
-                RowCtx rc;
-                if (live) rc = row_ctx(g, i, sorted_base);
+                TokMeta rc;
+                if (live) rc = tok_meta(g, i, sorted_base);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
@@ -459,41 +607,58 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     ptx::tc_fence_before();
     __syncthreads();
 
-    if (splits > 1) {
-        // ---- cluster split-K: reduce the partial tiles through DSMEM
-        ptx::cluster_sync();
+    if (!g.tok_on_p) {
+        // ---- features-on-P epilogue: sum the K-split partial tiles of the
+        // cluster (distributed shared memory; a cluster of one reads its own),
+        // then apply the slots to items of (token, 8 consecutive features)
+        if (splits > 1) ptx::cluster_sync();
         int any_abort = 0;
         const uint32_t red_base = ptx::smem_u32(smem);
+        const uint32_t redv_off = (uint32_t)(BN * TILE_M * 4);
         for (int r = 0; r < splits; ++r)
-            any_abort |= ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_u32(&ctrl->abort), (uint32_t)r));
+            any_abort |= splits > 1 ? ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_u32(&ctrl->abort), (uint32_t)r))
+                                    : ctrl->abort;
         if (!any_abort && warp >= 2) {
             const int et = threadIdx.x - 64;
             const int FR = TILE_M / splits;   // feature rows finalised by this CTA
-            const int fl = et % FR, tg = et / FR, TG = 128 / FR;
-            const int f = crank * FR + fl;
-            const int ft = tile0 % g.n_ft, tt = tile0 / g.n_ft;
-            const int j = ft * TILE_M + f;
+            const int G8 = FR / 8;            // 8-feature groups per token
+            const int ft = tile0 % g.n_ft;
+            const int R = g.lr_rmax;
+            const int nt = min(BN, n_tok);
             uint32_t rb[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) rb[r] = r < splits ? ptx::mapa(red_base, (uint32_t)r) : 0u;
-            if (j < g.n_feat) {
-                int last_i = -1;
-                RowCtx rc;
+            for (int r = 0; r < 8; ++r) rb[r] = r < splits ? (splits > 1 ? ptx::mapa(red_base, (uint32_t)r) : red_base) : 0u;
 #pragma unroll 1
-                for (int t = tg; t < BN; t += TG) {
-                    const int i = tt * BN + t;
-                    if (i >= n_tok) break;
-                    float sum = 0.f;
-                    const uint32_t off = (uint32_t)(t * TILE_M + f) * 4u;
+            for (int item = et; item < nt * G8; item += 128) {
+                const int t = item / G8, fg = item - t * G8;
+                const int f0 = crank * FR + fg * 8;
+                const int j0 = ft * TILE_M + f0;
+                if (j0 >= g.n_feat) continue;
+                const uint32_t off = (uint32_t)(t * TILE_M + f0) * 4u;
+                float acc[8], vacc[8];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        if (r < splits) sum += ptx::ld_dsmem_f32(rb[r] + off);
-                    if (i != last_i) { rc = row_ctx(g, i, sorted_base); last_i = i; }
-                    emit1(g, rc, j, sum);
+                for (int k = 0; k < 8; ++k) { acc[k] = 0.f; vacc[k] = 0.f; }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (r < splits) {
+                        const float4 a0 = ld_dsmem_f32x4(rb[r] + off), a1 = ld_dsmem_f32x4(rb[r] + off + 16);
+                        acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+                        acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
+                    }
                 }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (r < n_vera_ranks) {
+                        const float4 a0 = ld_dsmem_f32x4(rb[r] + redv_off + off);
+                        const float4 a1 = ld_dsmem_f32x4(rb[r] + redv_off + off + 16);
+                        vacc[0] += a0.x; vacc[1] += a0.y; vacc[2] += a0.z; vacc[3] += a0.w;
+                        vacc[4] += a1.x; vacc[5] += a1.y; vacc[6] += a1.z; vacc[7] += a1.w;
+                    }
+                }
+                emit8(g, tmeta[t], vtile + t * R, j0, acc, vacc);
             }
         }
-        ptx::cluster_sync();
+        if (splits > 1) ptx::cluster_sync();
     }
 
     if (warp == 1) {
@@ -538,7 +703,13 @@ cudaError_t launch_one(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bo
 
 }  // namespace
 
-GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms) {
+size_t gemm_smem_bytes(int bn, int stages, int lr_rmax) {
+    const size_t stage_bytes = (size_t)TILE_M * 128 + (size_t)bn * 128;
+    return 1024 + (size_t)stages * stage_bytes + CTRL_BYTES + (size_t)bn * sizeof(TokMeta) +
+           (size_t)bn * lr_rmax * sizeof(float);
+}
+
+GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms, int lr_rmax) {
     GemmPlan p{};
     p.tf32 = tf32 ? 1 : 0;
     if (tok_on_p) {
@@ -557,14 +728,16 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         const int per_sm = p.bn == 64 ? 2 : 1;
         const int target = per_sm * num_sms;
         p.stages = p.bn == 64 ? 4 : (p.bn == 128 ? 5 : 4);
+        // two CTAs of the 64-token tile share an SM: keep both within its shared memory
+        while (p.bn == 64 && p.stages > 2 && 2 * (gemm_smem_bytes(p.bn, p.stages, lr_rmax) + 1024) > 228 * 1024)
+            --p.stages;
         int s = 1;
         while (s < 8 && tiles * (s * 2) <= target && kblocks / (s * 2) >= 4) s *= 2;
         p.splits = s;
         p.grid = tiles * s;
     }
     if (p.grid < 1) p.grid = 1;
-    const int stage_bytes = TILE_M * 128 + p.bn * 128;
-    p.smem = 1024 + (size_t)p.stages * stage_bytes + CTRL_BYTES;
+    p.smem = gemm_smem_bytes(p.bn, p.stages, lr_rmax);
     return p;
 }
 

@@ -79,25 +79,43 @@ def call_bytes(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dty
                 e_b += 4 * d_out
     segments = len(seen) + (1 if has_base else 0)
 
-    kernels = [
-        # ids in; perm and sorted ids out; segment table; 22-int summary
-        ("index", 4 * n + 8 * n + 4 * (segments + 1) + 4 * segments + 88, 0),
-        # x in, perm/ids in, R of each distinct rotating adapter, x' out
-        ("rotate", n * d_in * E + 8 * n + R_b + n * kd * E, 2 * n_rot * d_in * 32),
-        # W, x', s/b vectors, perm/ids, out
-        ("base_gemm", d_out * kd * E + n * kd * E + sb_b + 8 * n + n * d_out * Eo, 2 * n * kd * d_out),
-    ]
-    if lowrank_launched:
-        ks = lowrank_ks(d_in)
-        kernels.append(("lr_shrink", n_lr * d_in * E + A_b + ks * lr_rank_rows * 4, 2 * lr_rank_rows * d_in))
-        kernels.append(("lr_expand", ks * lr_rank_rows * 4 + B_b + 2 * n_lr * d_out * Eo,
-                        2 * lr_rank_rows * d_out))
-    if vera_launched:
-        shA = rv * kd * E if n_v else 0
-        shB = d_out * krv * E if n_v else 0
-        kernels.append(("vera_shrink", n_v * kd * E + shA + d_b + n_v * krv * E, 2 * n_v * rv * kd))
-        kernels.append(("vera_expand", n_v * krv * E + shB + e_b + 2 * n_v * d_out * Eo,
-                        2 * n_v * krv * d_out))
+    # bf16 calls of at most 128 tokens follow the fused decode plan (one
+    # prologue launch and one GEMM launch); others launch one kernel per step
+    fused = dtype != "fp32" and n <= 128
+    index_out = 8 * n + 4 * (segments + 1) + 4 * segments + 88
+    if fused:
+        shA = rv * d_in * E if n_v else 0
+        shB = d_out * rv * E if n_v else 0
+        kernels = [
+            # ids; x once; R, A', shared A, d once each; x', v, U and the index out
+            ("prep", 4 * n + n * d_in * E + R_b + A_b + shA + d_b + n * kd * E + lr_rank_rows * 4
+             + n_v * rv * E + index_out,
+             2 * n_rot * d_in * 32 + 2 * lr_rank_rows * d_in + 2 * n_v * rv * d_in),
+            # W, x', s/b, B', v, shared B, U, e, perm/ids, out
+            ("base_gemm", d_out * kd * E + n * kd * E + sb_b + B_b + lr_rank_rows * 4 + shB + n_v * rv * E
+             + e_b + 8 * n + n * d_out * Eo,
+             2 * n * kd * d_out + 2 * lr_rank_rows * d_out + 2 * n_v * rv * d_out),
+        ]
+    else:
+        kernels = [
+            # ids in; perm and sorted ids out; segment table; 22-int summary
+            ("index", 4 * n + index_out, 0),
+            # x in, perm/ids in, R of each distinct rotating adapter, x' out
+            ("rotate", n * d_in * E + 8 * n + R_b + n * kd * E, 2 * n_rot * d_in * 32),
+            # W, x', s/b vectors, perm/ids, out
+            ("base_gemm", d_out * kd * E + n * kd * E + sb_b + 8 * n + n * d_out * Eo, 2 * n * kd * d_out),
+        ]
+        if lowrank_launched:
+            ks = lowrank_ks(d_in)
+            kernels.append(("lr_shrink", n_lr * d_in * E + A_b + ks * lr_rank_rows * 4, 2 * lr_rank_rows * d_in))
+            kernels.append(("lr_expand", ks * lr_rank_rows * 4 + B_b + 2 * n_lr * d_out * Eo,
+                            2 * lr_rank_rows * d_out))
+        if vera_launched:
+            shA = rv * kd * E if n_v else 0
+            shB = d_out * krv * E if n_v else 0
+            kernels.append(("vera_shrink", n_v * kd * E + shA + d_b + n_v * krv * E, 2 * n_v * rv * kd))
+            kernels.append(("vera_expand", n_v * krv * E + shB + e_b + 2 * n_v * d_out * Eo,
+                            2 * n_v * krv * d_out))
     shared = (d_in + d_out) * rv * E if n_v else 0
     W = d_in * d_out * E
     return {

@@ -115,24 +115,26 @@ def test_byte_model_matches_oracle(lib, name, make, layer, out_dtype):
         assert got[k] == ref[k], k
 
 
-def test_byte_model_hand_example(lib):
-    """Hand-counted bytes (tests/golden/byte_model_hand.json)."""
+@pytest.mark.parametrize("case", [0, 1])
+def test_byte_model_hand_example(lib, case):
+    """Hand-counted bytes (tests/golden/byte_model_hand.json), both launch plans."""
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "byte_model_hand.json")))
     ads = {int(k): v for k, v in g["adapters"].items()}
-    ref = OBM.call_bytes(g["ids"], ads, g["d_in"], g["d_out"], g["shared_rank"], g["dtype"], g["out_dtype"],
-                         g["lowrank_launched"], g["vera_launched"])
-    exp = g["expected"]
+    c = g["cases"][case]
+    ref = OBM.call_bytes(g["ids"], ads, c["d_in"], c["d_out"], c["shared_rank"], c["dtype"], c["out_dtype"],
+                         c["lowrank_launched"], c["vera_launched"])
+    exp = c["expected"]
     assert [list(k) for k in ref["kernels"]] == exp["kernels"]
     assert ref["algorithmic_bytes"] == exp["algorithmic_bytes"]
     assert ref["adapter_bytes"] == exp["adapter_bytes"]
 
     class W:
-        dtype = g["dtype"]
+        dtype = c["dtype"]
 
     class Lr:
-        d_in, d_out, shared_rank = g["d_in"], g["d_out"], g["shared_rank"]
-    got = _c_report(lib, W, Lr, ads, g["lowrank_launched"], g["vera_launched"], np.array(g["ids"]),
-                    g["out_dtype"], 8)
+        d_in, d_out, shared_rank = c["d_in"], c["d_out"], c["shared_rank"]
+    got = _c_report(lib, W, Lr, ads, c["lowrank_launched"], c["vera_launched"], np.array(g["ids"]),
+                    c["out_dtype"], 8)
     assert [list(k) for k in got["kernels"]] == exp["kernels"]
     assert got["algorithmic_bytes"] == exp["algorithmic_bytes"]
 

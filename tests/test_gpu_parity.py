@@ -97,9 +97,12 @@ def _small_decode(n=50):
     return WL.with_nf_adapters(WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES))
 
 
+@pytest.mark.parametrize("n", [50, 128, 200])
 @pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
-def test_small_decode_parity(scute, out_dtype):
-    w = _small_decode()
+def test_small_decode_parity(scute, out_dtype, n):
+    """n <= 128: fused decode path (one prologue + one GEMM launch);
+    128 < n <= 256: separate kernels, tokens on the tile's N side."""
+    w = _small_decode(n)
     ctx = H.make_ctx(scute, w)
     outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
     assert ctx.sync_status() == 0
