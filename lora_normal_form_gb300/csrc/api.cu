@@ -553,10 +553,19 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         pa.u_ld = L.krv;
         pa.Ash = L.Ash;
         pa.rv = vera_on ? L.rv : 0;
-        pa.n_rot = (L.d_in + 255) / 256;
+        // rotation items: per 256-column chunk, one copy item plus one item per
+        // rotated segment the batch can hold
+        const int rot_segs = L.n_rot < nn ? L.n_rot : nn;
+        pa.n_rot = ((L.d_in + 255) / 256) * (1 + rot_segs);
         pa.lr_groups = lr_rmax > 0 ? (lr_rmax + 3) / 4 : 1;
         pa.n_lr = lr_rmax > 0 ? (nn < L.n_lr ? nn : L.n_lr) * pa.lr_groups : 0;
         pa.n_vera = vera_on ? (L.rv + 3) / 4 : 0;
+        pa.pf_base[0] = L.Wt;
+        pa.pf_bytes[0] = (size_t)L.d_out * L.kdim * c->esz;
+        if (vera_on) {
+            pa.pf_base[1] = L.Bsh;
+            pa.pf_bytes[1] = (size_t)L.d_out * L.krv * c->esz;
+        }
         CU_TRY(c, launch_prep(pa, pa.n_rot + pa.n_lr + pa.n_vera, st, c->pdl));
         ++k;
     } else {

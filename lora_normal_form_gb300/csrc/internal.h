@@ -146,6 +146,10 @@ struct PrepArgs {
     const void *Ash;           // [rv, d_in] shared VeRA A, K-major
     int rv;
     int n_rot, n_lr, lr_groups, n_vera;   // work items per kind (grid = their sum)
+    // read-only regions of the GEMM that follows (its weights), prefetched
+    // into L2 while this prologue runs
+    const void *pf_base[2];
+    size_t pf_bytes[2];
 };
 size_t prep_smem_bytes();
 cudaError_t launch_prep(const PrepArgs &p, int grid, cudaStream_t st, bool pdl);

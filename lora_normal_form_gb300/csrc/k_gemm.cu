@@ -554,6 +554,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                 }
             }
             epi_bar();
+            // warm L2 with the epilogue's per-token operands of this CTA's items
+            // while the K loop streams the weights
+            {
+                const int FR = TILE_M / splits, G8 = FR / 8;
+                const int ft = tile0 % g.n_ft;
+                const int nt = min(BN, n_tok);
+                for (int item = et; item < nt * G8; item += 128) {
+                    const int t = item / G8, fg = item - t * G8;
+                    const int j0 = ft * TILE_M + crank * FR + fg * 8;
+                    if (j0 >= g.n_feat) continue;
+                    const TokMeta &m = tmeta[t];
+                    if (m.v1) ptx::prefetch_l2(m.v1 + j0);
+                    if (m.v2) ptx::prefetch_l2(m.v2 + j0);
+                    if (m.ve) ptx::prefetch_l2(m.ve + j0);
+                    if (m.B) {
+                        const __nv_bfloat16 *B = reinterpret_cast<const __nv_bfloat16 *>(m.B) + j0;
+                        for (int q = 0; q < m.rank; ++q) ptx::prefetch_l2(B + (size_t)q * g.n_feat);
+                    }
+                }
+            }
         }
         int acc = 0;
         uint32_t acc_phase = 0;

@@ -5,8 +5,9 @@
 // shared memory (key = (method, adapter id), ties in token order: the same
 // stable grouping the stand-alone indexing kernel produces), then serves one
 // work item:
-//   * gather / rotate   x'[i] = x[perm[i]] R_a for OFT rows, a copy otherwise,
-//                       one 256-column chunk per CTA (article "Scute: Exact
+//   * gather / rotate   x'[i] = x[perm[i]] R_a for OFT rows, a copy otherwise;
+//                       per 256-column chunk one CTA copies the unrotated rows
+//                       and one CTA per rotated segment rotates its rows (article "Scute: Exact
 //                       Batched Serving for PEFT Adapters Beyond LoRA",
 //                       paper-daily.com, section "Where is the cheapest place
 //                       to compute the remaining slots?": OFT's rotation runs
@@ -70,6 +71,7 @@ struct PrepSmem {
     int seg_rank[PREP_MAX_TOKENS];
     const void *row_R[PREP_MAX_TOKENS]; // rotation of each sorted row (null = copy)
     int seg_lr[PREP_MAX_TOKENS];        // segment has an owned low-rank term
+    int row_lr[PREP_MAX_TOKENS];        // sorted row's adapter has an owned term
     int warp_tot[33];
     int count[N_RANKS], offset[N_RANKS], segc[N_RANKS];
     int n_seg, bad;
@@ -139,17 +141,45 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
     const uint32_t A = (uint32_t)p.A;
     const uint32_t base_key = (uint32_t)RANK_BASE * A;
 
+    // The weights of the GEMM that follows do not depend on any earlier
+    // kernel: start pulling this CTA's share of them into L2 before waiting.
+    if (tid == 0) {
+        for (int r = 0; r < 2; ++r) {
+            const size_t bytes = p.pf_bytes[r];
+            if (!p.pf_base[r] || bytes == 0) continue;
+            size_t share = (bytes + gridDim.x - 1) / gridDim.x;
+            share = (share + 4095) & ~(size_t)4095;
+            size_t beg = (size_t)blockIdx.x * share;
+            const size_t end = beg + share < bytes ? beg + share : bytes;
+            const uint8_t *base = reinterpret_cast<const uint8_t *>(p.pf_base[r]);
+            while (beg < end) {
+                const size_t len = end - beg < 65536 ? end - beg : 65536;
+                ptx::bulk_prefetch_l2(base + beg, (uint32_t)(len & ~(size_t)15));
+                beg += len;
+            }
+        }
+    }
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
 
     // ---- order the ids (every CTA): rank of each token among (key, token)
     if (tid == 0) sm.bad = 0;
     if (tid < N_RANKS) { sm.count[tid] = 0; sm.segc[tid] = 0; }
+    // the id's method and its slot pointers are fetched together (one round
+    // of dependent loads), then carried to the token's sorted row
+    const void *tR = nullptr;
+    int t_lr = 0;
     if (tid < n) {
         const int id = p.ids[tid];
         int m = -1;
-        if (id >= 0 && id < p.A) m = p.method_tab[id];
+        if (id >= 0 && id < p.A) {
+            m = p.method_tab[id];
+            const Slot &sl = p.slots[id];
+            tR = sl.R;
+            t_lr = sl.A != nullptr && sl.rank > 0;
+        }
         if (m < 0 && id != -1) sm.bad = 1;
+        if (m < 0) { tR = nullptr; t_lr = 0; }
         sm.key[tid] = m >= 0 ? (uint32_t)m * A + (uint32_t)id : base_key;
     }
     __syncthreads();
@@ -162,6 +192,8 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         }
         sm.perm[r] = tid;
         sm.skey[r] = kt;
+        sm.row_R[r] = tR;
+        sm.row_lr[r] = t_lr;
     }
     __syncthreads();
     // segments: runs of one key in sorted order
@@ -185,13 +217,12 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         rank = (int)(k / A);
         aid = rank >= RANK_BASE ? -1 : (int)(k - (uint32_t)rank * A);
         atomicAdd(&sm.count[rank], 1);
-        sm.row_R[tid] = aid >= 0 ? p.slots[aid].R : nullptr;
         if (head) {
             const int s = sm.warp_tot[w] + incl - 1;
             sm.seg_start[s] = tid;
             sm.seg_aid[s] = aid;
             sm.seg_rank[s] = rank;
-            sm.seg_lr[s] = aid >= 0 && p.slots[aid].A != nullptr && p.slots[aid].rank > 0;
+            sm.seg_lr[s] = sm.row_lr[tid];
             atomicAdd(&sm.segc[rank], 1);
         }
     }
@@ -231,59 +262,67 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
 
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(p.x);
     if (b < p.n_rot) {
-        // ================= gather / rotate one 256-column chunk of every row
-        const int col0 = b * 256;
+        // ================= gather / rotate: item = (256-column chunk, part);
+        // part 0 copies every unrotated row of the chunk, part k >= 1 rotates
+        // the k-th rotated segment (one adapter's rows) of the chunk
+        const int chunks = (p.d_in + 255) / 256;
+        const int chunk = b % chunks, part = b / chunks;
+        const int col0 = chunk * 256;
         const int ncols = min(256, p.d_in - col0);
         __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(p.xs);
-        // copies: 32 threads x 8 columns per row, 8 rows at a time
-        for (int i = w; i < n; i += PREP_THREADS / 32) {
-            if (sm.row_R[i] != nullptr) continue;
-            const int c = lane * 8;
-            if (c < ncols)
-                *reinterpret_cast<uint4 *>(xs + (size_t)i * p.kdim + col0 + c) =
-                    *reinterpret_cast<const uint4 *>(x + (size_t)sm.perm[i] * p.d_in + col0 + c);
+        if (part == 0) {
+            // 32 threads x 8 columns per row, 8 rows at a time
+            for (int i = w; i < n; i += PREP_THREADS / 32) {
+                if (sm.row_R[i] != nullptr) continue;
+                const int c = lane * 8;
+                if (c < ncols)
+                    *reinterpret_cast<uint4 *>(xs + (size_t)i * p.kdim + col0 + c) =
+                        *reinterpret_cast<const uint4 *>(x + (size_t)sm.perm[i] * p.d_in + col0 + c);
+            }
+            return;
         }
-        // rotations, one adapter segment at a time (its rows are contiguous):
-        // R's 8 blocks of this chunk and up to ROT_ROWS rows of x are staged
-        // with 16-byte loads, then every thread produces one column per row
+        int seg = -1, seen = 0;
         for (int sgi = 0; sgi < sm.n_seg; ++sgi) {
-            const int s0 = sm.seg_start[sgi], s1 = sm.seg_start[sgi + 1];
-            const void *Rv = sm.row_R[s0];
-            if (Rv == nullptr) continue;
-            const __nv_bfloat16 *Rb =
-                reinterpret_cast<const __nv_bfloat16 *>(Rv) + (size_t)(col0 / OFT_BLK) * OFT_BLK * OFT_BLK;
-            const int nvec = (ncols / OFT_BLK) * OFT_BLK * OFT_BLK / 8;
-            for (int e = tid; e < nvec; e += PREP_THREADS) {
+            if (sm.row_R[sm.seg_start[sgi]] == nullptr) continue;
+            if (++seen == part) { seg = sgi; break; }
+        }
+        if (seg < 0) return;
+        const int s0 = sm.seg_start[seg], s1 = sm.seg_start[seg + 1];
+        const __nv_bfloat16 *Rb = reinterpret_cast<const __nv_bfloat16 *>(sm.row_R[s0]) +
+                                  (size_t)(col0 / OFT_BLK) * OFT_BLK * OFT_BLK;
+        const int nvec = (ncols / OFT_BLK) * OFT_BLK * OFT_BLK / 8;
+        for (int e = tid; e < nvec; e += PREP_THREADS) {
+            float v[8];
+            load8(Rb + (size_t)e * 8, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) (&sm.R[0][0][0])[e * 8 + q] = v[q];
+        }
+        // R's 8 blocks of this chunk and up to ROT_ROWS rows of x are staged
+        // with 16-byte loads; every thread then produces one column per row
+        for (int r0 = s0; r0 < s1; r0 += ROT_ROWS) {
+            const int nr = min(ROT_ROWS, s1 - r0);
+            for (int e = tid; e < nr * 32; e += PREP_THREADS) {
+                const int rr = e >> 5, c = (e & 31) * 8;
                 float v[8];
-                load8(Rb + (size_t)e * 8, v);
+                if (c < ncols) load8(x + (size_t)sm.perm[r0 + rr] * p.d_in + col0 + c, v);
+                else
 #pragma unroll
-                for (int q = 0; q < 8; ++q) (&sm.R[0][0][0])[e * 8 + q] = v[q];
+                    for (int q = 0; q < 8; ++q) v[q] = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) sm.xrows[rr][c + q] = v[q];
             }
-            for (int r0 = s0; r0 < s1; r0 += ROT_ROWS) {
-                const int nr = min(ROT_ROWS, s1 - r0);
-                for (int e = tid; e < nr * 32; e += PREP_THREADS) {
-                    const int rr = e >> 5, c = (e & 31) * 8;
-                    float v[8];
-                    if (c < ncols) load8(x + (size_t)sm.perm[r0 + rr] * p.d_in + col0 + c, v);
-                    else
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) v[q] = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) sm.xrows[rr][c + q] = v[q];
-                }
-                __syncthreads();
-                if (tid < ncols) {
-                    const int blk = tid >> 5, cc = tid & 31;
-                    for (int rr = 0; rr < nr; ++rr) {
-                        float acc = 0.f;
+            __syncthreads();
+            if (tid < ncols) {
+                const int blk = tid >> 5, cc = tid & 31;
+                for (int rr = 0; rr < nr; ++rr) {
+                    float acc = 0.f;
 #pragma unroll 8
-                        for (int m = 0; m < OFT_BLK; ++m)
-                            acc = fmaf(sm.xrows[rr][blk * OFT_BLK + m], sm.R[blk][m][cc], acc);
-                        xs[(size_t)(r0 + rr) * p.kdim + col0 + tid] = __float2bfloat16_rn(acc);
-                    }
+                    for (int m = 0; m < OFT_BLK; ++m)
+                        acc = fmaf(sm.xrows[rr][blk * OFT_BLK + m], sm.R[blk][m][cc], acc);
+                    xs[(size_t)(r0 + rr) * p.kdim + col0 + tid] = __float2bfloat16_rn(acc);
                 }
-                __syncthreads();
             }
+            __syncthreads();
         }
         return;
     }

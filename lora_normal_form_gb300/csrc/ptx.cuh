@@ -148,6 +148,15 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+// Asynchronous bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, size a
+// multiple of 16); no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------ programmatic dependent launch
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() {
