@@ -160,7 +160,8 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               cudaMemset(c->d_status, 0, sizeof(int)) == cudaSuccess &&
               cudaMalloc(&c->d_err, sizeof(int)) == cudaSuccess &&
               cudaMalloc(&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
-              cudaMalloc(&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess;
+              cudaMalloc(&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess &&
+              cudaMalloc(&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess;
     if (!ok) {
         scute_destroy(c);
         return SCUTE_ERR_OOM;
@@ -181,7 +182,7 @@ void scute_destroy(scute_ctx *c) {
     for (auto &a : c->adapters)
         if (a.storage) cudaFree(a.storage);
     void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid,
-                    c->d_meta, c->d_status, c->d_err, c->v_part, c->xs, c->U, c->st_x,
+                    c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
                     c->st_out, c->st_ids, c->tmp};
     for (void *p : bufs)
         if (p) cudaFree(p);
@@ -560,12 +561,6 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         pa.lr_groups = lr_rmax > 0 ? (lr_rmax + 3) / 4 : 1;
         pa.n_lr = lr_rmax > 0 ? (nn < L.n_lr ? nn : L.n_lr) * pa.lr_groups : 0;
         pa.n_vera = vera_on ? (L.rv + 3) / 4 : 0;
-        pa.pf_base[0] = L.Wt;
-        pa.pf_bytes[0] = (size_t)L.d_out * L.kdim * c->esz;
-        if (vera_on) {
-            pa.pf_base[1] = L.Bsh;
-            pa.pf_bytes[1] = (size_t)L.d_out * L.krv * c->esz;
-        }
         CU_TRY(c, launch_prep(pa, pa.n_rot + pa.n_lr + pa.n_vera, st, c->pdl));
         ++k;
     } else {
@@ -596,6 +591,11 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     g.aid_s = c->d_aid;
     g.out = out;
     g.status = c->d_status;
+    if (!tok_on_p) {
+        g.p_base = L.Wt;
+        g.p_pitch = (long long)L.kdim * c->esz;
+        g.p_rows = L.d_out;
+    }
     if (fused) {
         if (lr_rmax > 0) {
             g.v = c->v_part;
@@ -612,9 +612,13 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     g.splits = p.splits;
     g.stages = p.stages;
     g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
-    if (!tok_on_p &&
-        (size_t)p.stages * (128 * 128 + p.bn * 128) < (size_t)(g.vera_kb ? 2 : 1) * p.bn * 128 * 4)
-        return fail(c, SCUTE_ERR_UNSUPPORTED, "split-K partial tiles do not fit the pipeline buffers");
+    if (!tok_on_p && p.splits == 1 &&
+        (size_t)p.stages * (128 * 128 + p.bn * 128) < (size_t)(g.vera_kb ? 2 : 1) * p.bn * 132 * 4)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "the accumulator tile does not fit the pipeline buffers");
+    if (!tok_on_p && p.splits > 1 && gemm_part_floats(p.grid, p.bn, g.vera_kb > 0) > PART_WORKSPACE_FLOATS)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "K-split workspace too small for this launch");
+    g.part = c->gpart;
+    g.part_stride = (long long)p.bn * 128 * (g.vera_kb ? 2 : 1);
     const int slot = c->t_next;
     unsigned ev_flags = cudaEventRecordDefault;
     if (c->timing) {
@@ -667,6 +671,8 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         GemmPlan pv = plan_gemm(nn, L.rv, v.kblocks, tok_on_p, f32, c->num_sms);
         v.splits = pv.splits;
         v.stages = pv.stages;
+        v.part = c->gpart;
+        v.part_stride = (long long)pv.bn * 128;
         v.n_ft = tok_on_p ? (L.rv + pv.bn - 1) / pv.bn : (L.rv + 127) / 128;
         CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
 
@@ -683,6 +689,8 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         GemmPlan pe = plan_gemm(nn, L.d_out, e.kblocks, tok_on_p, f32, c->num_sms);
         e.splits = pe.splits;
         e.stages = pe.stages;
+        e.part = c->gpart;
+        e.part_stride = (long long)pe.bn * 128;
         e.n_ft = tok_on_p ? (L.d_out + pe.bn - 1) / pe.bn : (L.d_out + 127) / 128;
         CU_TRY(c, launch_gemm(e, pe, st, c->pdl));
         k += 2;

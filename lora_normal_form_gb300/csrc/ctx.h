@@ -64,6 +64,7 @@ struct scute_ctx {
     int *d_status = nullptr;
     int *d_err = nullptr;
     float *v_part = nullptr;
+    float *gpart = nullptr;      // K-split partial tiles of the GEMM
     void *xs = nullptr;
     size_t xs_cols = 0;  // elements per row the xs buffer holds
     void *U = nullptr;

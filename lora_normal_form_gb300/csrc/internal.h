@@ -83,7 +83,22 @@ struct GemmArgs {
     const float *v;            // owned low-rank intermediate [tokens][v_ld] (null = none)
     int v_ld;
     int lr_rmax;               // largest owned rank on the layer (v columns preloaded)
+    // the P operand's rows in global memory (features-on-P orientation): each
+    // CTA asks L2 for its whole K range of them at start
+    const void *p_base;
+    long long p_pitch;         // bytes between rows
+    int p_rows;
+    // K-split partial tiles: CTA b of a cluster writes [token][128] fp32 (and
+    // the VeRA plane after it) at part + b * part_stride; the cluster's CTAs
+    // then read each other's slices from L2
+    float *part;
+    long long part_stride;     // floats per CTA
 };
+// floats of K-split workspace one GEMM launch needs
+inline size_t gemm_part_floats(int grid, int bn, bool vera) {
+    return (size_t)grid * (size_t)bn * 128 * (vera ? 2 : 1);
+}
+constexpr size_t PART_WORKSPACE_FLOATS = (size_t)8 << 20;   // 32 MiB
 
 struct GemmPlan {
     int bn;        // 64, 128 or 256
@@ -146,10 +161,6 @@ struct PrepArgs {
     const void *Ash;           // [rv, d_in] shared VeRA A, K-major
     int rv;
     int n_rot, n_lr, lr_groups, n_vera;   // work items per kind (grid = their sum)
-    // read-only regions of the GEMM that follows (its weights), prefetched
-    // into L2 while this prologue runs
-    const void *pf_base[2];
-    size_t pf_bytes[2];
 };
 size_t prep_smem_bytes();
 cudaError_t launch_prep(const PrepArgs &p, int grid, cudaStream_t st, bool pdl);

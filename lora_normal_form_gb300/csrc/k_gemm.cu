@@ -40,6 +40,9 @@ constexpr int BOX_ROWS = 64;
 constexpr int BOX_BYTES = BOX_ROWS * 128;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 constexpr int CTRL_BYTES = 256;
+// token stride of the partial tiles in shared memory: 128 features plus 4
+// floats of padding, so the tokens a warp reads start on different banks
+constexpr int RED_LD = TILE_M + 4;
 
 // Shared-memory matrix descriptor for a K-major tile in the canonical
 // 128-byte-swizzle layout that TMA writes: rows of 128 bytes, 8-row atoms of
@@ -284,15 +287,15 @@ __device__ __forceinline__ void emit8(const GemmArgs &g, const TokMeta &m, const
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = acc[k] * s8[k] + b8[k];
         if (m.B) {
-            // owned low-rank expand: y += v_t B'[:, j0:j0+8], 16 ranks per batch of loads
+            // owned low-rank expand: y += v_t B'[:, j0:j0+8], 8 ranks per batch of loads
             const __nv_bfloat16 *B = reinterpret_cast<const __nv_bfloat16 *>(m.B) + j0;
-            for (int q0 = 0; q0 < m.rank; q0 += 16) {
-                uint4 bq[16];
+            for (int q0 = 0; q0 < m.rank; q0 += 8) {
+                uint4 bq[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
+                for (int q = 0; q < 8; ++q)
                     if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(B + (size_t)(q0 + q) * g.n_feat));
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     if (q0 + q < m.rank) {
                         const float vq = vrow[q0 + q];
                         const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&bq[q]);
@@ -359,12 +362,14 @@ __device__ __forceinline__ void emit8(const GemmArgs &g, const TokMeta &m, const
     }
 }
 
+// Plain load from a cluster peer's shared memory.  No memory clobber: the
+// cluster barriers around the reduction order it, and loads without one can be
+// issued back to back.
 __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 
@@ -445,6 +450,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             uint32_t phase = 0;
             long long issued = 0;
             bool dep_done = sched_dep;
+            if (g.p_base && !g.tok_on_p && splits > 0) {
+                // the weights do not depend on earlier kernels: ask L2 for this
+                // CTA's whole K range of its 128 rows now, so the ring below
+                // finds them there instead of waiting on DRAM stage by stage
+                const int prow0 = (tile0 % g.n_ft) * TILE_M;
+                const long long off = (long long)kb0 * 128;
+                long long want = (long long)(kb1 - kb0) * 128;
+                if (off + want > g.p_pitch) want = g.p_pitch - off;   // ragged K tail stays inside the row
+                const uint32_t bytes = want > 0 ? (uint32_t)(want & ~15ll) : 0u;
+                const uint8_t *base = reinterpret_cast<const uint8_t *>(g.p_base) + off;
+                for (int r = 0; bytes && r < TILE_M && prow0 + r < g.p_rows; ++r)
+                    ptx::bulk_prefetch_l2(base + (size_t)(prow0 + r) * g.p_pitch, bytes);
+            }
             for (int tile = tile0; tile < n_tiles; tile += tstep) {
                 const int ft = tile % g.n_ft, tt = tile / g.n_ft;
                 const int prow = g.tok_on_p ? tok_base + tt * TILE_M : ft * TILE_M;
@@ -584,21 +602,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const uint32_t tbv = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)BN;
             if (!g.tok_on_p) {
-                // features on rows, tokens on columns: the (partial) tile goes to
-                // this CTA's shared memory as [token][128 features]; the
-                // reduction and the epilogue run after the block-wide barrier
-                float *red = reinterpret_cast<float *>(smem);
-                float *redv = red + BN * TILE_M;
+                // features on rows, tokens on columns.  The (partial) tile is
+                // written as [token][128 features]: to shared memory when the
+                // CTA owns all of K, else to this CTA's slot of the workspace
+                // for the cluster's reduction through L2
+                float *red = splits > 1 ? g.part + (size_t)blockIdx.x * g.part_stride
+                                        : reinterpret_cast<float *>(smem);
+                const int ld = splits > 1 ? TILE_M : RED_LD;
+                float *redv = red + BN * ld;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     ptx::tmem_ld32(tb + c * 32, v);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) red[(c * 32 + k) * TILE_M + row] = v[k];
+                    for (int k = 0; k < 32; ++k) red[(c * 32 + k) * ld + row] = v[k];
                     if (my_vera) {
                         ptx::tmem_ld32(tbv + c * 32, v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) redv[(c * 32 + k) * TILE_M + row] = v[k];
+                        for (int k = 0; k < 32; ++k) redv[(c * 32 + k) * ld + row] = v[k];
                     }
                 }
             } else {
@@ -628,16 +649,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     __syncthreads();
 
     if (!g.tok_on_p) {
-        // ---- features-on-P epilogue: sum the K-split partial tiles of the
-        // cluster (distributed shared memory; a cluster of one reads its own),
-        // then apply the slots to items of (token, 8 consecutive features)
+        // ---- features-on-P epilogue: sum the cluster's K-split partial tiles
+        // (written to the workspace before the cluster barrier, which orders
+        // them at cluster scope), then apply the slots to items of (token,
+        // 8 consecutive features)
         if (splits > 1) ptx::cluster_sync();
         int any_abort = 0;
-        const uint32_t red_base = ptx::smem_u32(smem);
-        const uint32_t redv_off = (uint32_t)(BN * TILE_M * 4);
-        for (int r = 0; r < splits; ++r)
-            any_abort |= splits > 1 ? ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_u32(&ctrl->abort), (uint32_t)r))
-                                    : ctrl->abort;
+        {
+            int ab[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                ab[r] = r < splits ? (splits > 1 ? ptx::ld_dsmem_s32(ptx::mapa(ptx::smem_u32(&ctrl->abort), (uint32_t)r))
+                                                 : ctrl->abort)
+                                   : 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) any_abort |= ab[r];
+        }
+        // the peers' abort flags were the last reads of their shared memory
+        if (splits > 1) ptx::cluster_arrive_relaxed();
         if (!any_abort && warp >= 2) {
             const int et = threadIdx.x - 64;
             const int FR = TILE_M / splits;   // feature rows finalised by this CTA
@@ -645,40 +674,56 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             const int ft = tile0 % g.n_ft;
             const int R = g.lr_rmax;
             const int nt = min(BN, n_tok);
-            uint32_t rb[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) rb[r] = r < splits ? (splits > 1 ? ptx::mapa(red_base, (uint32_t)r) : red_base) : 0u;
+            const int ld = splits > 1 ? TILE_M : RED_LD;
+            const float *base0 = splits > 1 ? g.part + (size_t)(blockIdx.x - crank) * g.part_stride
+                                            : reinterpret_cast<const float *>(smem);
+            const size_t vstride = (size_t)BN * ld;
 #pragma unroll 1
             for (int item = et; item < nt * G8; item += 128) {
                 const int t = item / G8, fg = item - t * G8;
                 const int f0 = crank * FR + fg * 8;
                 const int j0 = ft * TILE_M + f0;
                 if (j0 >= g.n_feat) continue;
-                const uint32_t off = (uint32_t)(t * TILE_M + f0) * 4u;
+                const size_t off = (size_t)t * ld + f0;
+                // partial tiles of the cluster are loaded four ranks at a time,
+                // all loads of a batch before any add, so their latencies overlap
                 float acc[8], vacc[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) { acc[k] = 0.f; vacc[k] = 0.f; }
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (r < splits) {
-                        const float4 a0 = ld_dsmem_f32x4(rb[r] + off), a1 = ld_dsmem_f32x4(rb[r] + off + 16);
-                        acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
-                        acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
-                    }
-                }
+                for (int h = 0; h < 2; ++h) {
+                    float4 pb[8], pv[8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    if (r < n_vera_ranks) {
-                        const float4 a0 = ld_dsmem_f32x4(rb[r] + redv_off + off);
-                        const float4 a1 = ld_dsmem_f32x4(rb[r] + redv_off + off + 16);
-                        vacc[0] += a0.x; vacc[1] += a0.y; vacc[2] += a0.z; vacc[3] += a0.w;
-                        vacc[4] += a1.x; vacc[5] += a1.y; vacc[6] += a1.z; vacc[7] += a1.w;
+                    for (int u = 0; u < 4; ++u) {
+                        const int r = h * 4 + u;
+                        const float4 *src = reinterpret_cast<const float4 *>(base0 + (size_t)r * g.part_stride + off);
+                        const float4 *srcv = reinterpret_cast<const float4 *>(base0 + (size_t)r * g.part_stride + off + vstride);
+                        if (splits == 1) {
+                            // the tile is in this CTA's shared memory
+                            if (r == 0) { pb[0] = src[0]; pb[1] = src[1]; }
+                            if (r < n_vera_ranks) { pv[2 * u] = srcv[0]; pv[2 * u + 1] = srcv[1]; }
+                        } else {
+                            // peers' slices in L2 (never cached in this SM's L1)
+                            if (r < splits) { pb[2 * u] = __ldcg(src); pb[2 * u + 1] = __ldcg(src + 1); }
+                            if (r < n_vera_ranks) { pv[2 * u] = __ldcg(srcv); pv[2 * u + 1] = __ldcg(srcv + 1); }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int r = h * 4 + u;
+                        if (r < splits) {
+                            acc[0] += pb[2 * u].x; acc[1] += pb[2 * u].y; acc[2] += pb[2 * u].z; acc[3] += pb[2 * u].w;
+                            acc[4] += pb[2 * u + 1].x; acc[5] += pb[2 * u + 1].y; acc[6] += pb[2 * u + 1].z; acc[7] += pb[2 * u + 1].w;
+                        }
+                        if (r < n_vera_ranks) {
+                            vacc[0] += pv[2 * u].x; vacc[1] += pv[2 * u].y; vacc[2] += pv[2 * u].z; vacc[3] += pv[2 * u].w;
+                            vacc[4] += pv[2 * u + 1].x; vacc[5] += pv[2 * u + 1].y; vacc[6] += pv[2 * u + 1].z; vacc[7] += pv[2 * u + 1].w;
+                        }
                     }
                 }
                 emit8(g, tmeta[t], vtile + t * R, j0, acc, vacc);
             }
         }
-        if (splits > 1) ptx::cluster_sync();
     }
 
     if (warp == 1) {
@@ -686,6 +731,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
         ptx::tmem_dealloc(tmem_base, NCOLS);
     }
     if (threadIdx.x == 0 && ctrl->abort) atomicOr(g.status, STATUS_TIMEOUT);
+    if (!g.tok_on_p && splits > 1) ptx::cluster_wait();
 }
 
 template <int BN, bool TF32>

@@ -31,7 +31,7 @@ namespace scute {
 namespace {
 
 constexpr int PREP_THREADS = 256;
-constexpr int SHRINK_ROWS = 16;   // rows per pass of the shrink
+constexpr int SHRINK_ROWS = 4;    // rows per pass of the shrink
 constexpr int SHRINK_Q = 4;       // ranks per shrink work item
 constexpr int ROT_ROWS = 16;      // rows rotated per batch
 
@@ -75,26 +75,31 @@ struct PrepSmem {
     int warp_tot[33];
     int count[N_RANKS], offset[N_RANKS], segc[N_RANKS];
     int n_seg, bad;
-    float red[PREP_THREADS / 32][SHRINK_ROWS * SHRINK_Q];
+    float red[PREP_THREADS / 32][32];
+    const float *row_vd[PREP_MAX_TOKENS]; // VeRA d of each sorted row
     float R[8][OFT_BLK][OFT_BLK];
     float xrows[ROT_ROWS][256];
 };
 
 // x_i A_rows^T for up to 4 rows of A (each [d_in], bf16) and the sorted rows
-// [r0, r1); emit(i, q, value) is called by one thread per (row, q).
+// [r0, r1); emit(i, q, value) is called by one thread per (row, q).  Each
+// thread covers 8 consecutive k per pass, loading its A and x vectors before
+// any multiply; a warp then reduces its 16 partial sums (4 rows x 4 ranks)
+// with a transposing butterfly (16 shuffles) so that lanes 2s and 2s+1 hold
+// sum s, and the 8 warps' sums are added in a fixed order.
 template <typename Emit>
 __device__ void shrink(const __nv_bfloat16 *x, int d_in, const int *perm, int r0, int r1,
                        const __nv_bfloat16 *Arows, int nq, PrepSmem &sm, Emit emit) {
+    constexpr int NV = SHRINK_ROWS * SHRINK_Q;   // 16
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     for (int rc = r0; rc < r1; rc += SHRINK_ROWS) {
         const int nr = min(SHRINK_ROWS, r1 - rc);
-        float acc[SHRINK_ROWS][SHRINK_Q];
+        float v[NV];
 #pragma unroll
-        for (int r = 0; r < SHRINK_ROWS; ++r)
-#pragma unroll
-            for (int q = 0; q < SHRINK_Q; ++q) acc[r][q] = 0.f;
+        for (int i = 0; i < NV; ++i) v[i] = 0.f;
+#pragma unroll 2
         for (int k = tid * 8; k < d_in; k += PREP_THREADS * 8) {
-            float a[SHRINK_Q][8];
+            float a[SHRINK_Q][8], xv[SHRINK_ROWS][8];
 #pragma unroll
             for (int q = 0; q < SHRINK_Q; ++q) {
                 if (q < nq) load8(Arows + (size_t)q * d_in + k, a[q]);
@@ -104,25 +109,33 @@ __device__ void shrink(const __nv_bfloat16 *x, int d_in, const int *perm, int r0
             }
 #pragma unroll
             for (int r = 0; r < SHRINK_ROWS; ++r) {
-                if (r < nr) {
-                    float xv[8];
-                    load8(x + (size_t)perm[rc + r] * d_in + k, xv);
+                if (r < nr) load8(x + (size_t)perm[rc + r] * d_in + k, xv[r]);
+                else
 #pragma unroll
-                    for (int q = 0; q < SHRINK_Q; ++q)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[r][q] = fmaf(xv[e], a[q][e], acc[r][q]);
-                }
+                    for (int e = 0; e < 8; ++e) xv[r][e] = 0.f;
             }
+#pragma unroll
+            for (int r = 0; r < SHRINK_ROWS; ++r)
+#pragma unroll
+                for (int q = 0; q < SHRINK_Q; ++q)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[r * SHRINK_Q + q] = fmaf(xv[r][e], a[q][e], v[r * SHRINK_Q + q]);
         }
 #pragma unroll
-        for (int r = 0; r < SHRINK_ROWS; ++r)
+        for (int st = 0; st < 4; ++st) {
+            const int o = 16 >> st, half = 8 >> st;
+            const bool upper = (lane & o) != 0;
 #pragma unroll
-            for (int q = 0; q < SHRINK_Q; ++q) {
-                const float s = warp_sum(acc[r][q]);
-                if (lane == 0) sm.red[w][r * SHRINK_Q + q] = s;
+            for (int i = 0; i < half; ++i) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        if ((lane & 1) == 0) sm.red[w][lane >> 1] = v[0];
         __syncthreads();
-        if (tid < SHRINK_ROWS * SHRINK_Q) {
+        if (tid < NV) {
             const int r = tid / SHRINK_Q, q = tid % SHRINK_Q;
             float s = 0.f;
 #pragma unroll
@@ -133,7 +146,7 @@ __device__ void shrink(const __nv_bfloat16 *x, int d_in, const int *perm, int r0
     }
 }
 
-__global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constant__ PrepArgs p) {
+__global__ void __launch_bounds__(PREP_THREADS, 2) prep_kernel(const __grid_constant__ PrepArgs p) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &sm = *reinterpret_cast<PrepSmem *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -141,24 +154,6 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
     const uint32_t A = (uint32_t)p.A;
     const uint32_t base_key = (uint32_t)RANK_BASE * A;
 
-    // The weights of the GEMM that follows do not depend on any earlier
-    // kernel: start pulling this CTA's share of them into L2 before waiting.
-    if (tid == 0) {
-        for (int r = 0; r < 2; ++r) {
-            const size_t bytes = p.pf_bytes[r];
-            if (!p.pf_base[r] || bytes == 0) continue;
-            size_t share = (bytes + gridDim.x - 1) / gridDim.x;
-            share = (share + 4095) & ~(size_t)4095;
-            size_t beg = (size_t)blockIdx.x * share;
-            const size_t end = beg + share < bytes ? beg + share : bytes;
-            const uint8_t *base = reinterpret_cast<const uint8_t *>(p.pf_base[r]);
-            while (beg < end) {
-                const size_t len = end - beg < 65536 ? end - beg : 65536;
-                ptx::bulk_prefetch_l2(base + beg, (uint32_t)(len & ~(size_t)15));
-                beg += len;
-            }
-        }
-    }
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
 
@@ -168,6 +163,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
     // the id's method and its slot pointers are fetched together (one round
     // of dependent loads), then carried to the token's sorted row
     const void *tR = nullptr;
+    const float *tvd = nullptr;
     int t_lr = 0;
     if (tid < n) {
         const int id = p.ids[tid];
@@ -176,10 +172,11 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
             m = p.method_tab[id];
             const Slot &sl = p.slots[id];
             tR = sl.R;
+            tvd = sl.vd;
             t_lr = sl.A != nullptr && sl.rank > 0;
         }
         if (m < 0 && id != -1) sm.bad = 1;
-        if (m < 0) { tR = nullptr; t_lr = 0; }
+        if (m < 0) { tR = nullptr; tvd = nullptr; t_lr = 0; }
         sm.key[tid] = m >= 0 ? (uint32_t)m * A + (uint32_t)id : base_key;
     }
     __syncthreads();
@@ -193,6 +190,7 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         sm.perm[r] = tid;
         sm.skey[r] = kt;
         sm.row_R[r] = tR;
+        sm.row_vd[r] = tvd;
         sm.row_lr[r] = t_lr;
     }
     __syncthreads();
@@ -271,13 +269,23 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         const int ncols = min(256, p.d_in - col0);
         __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(p.xs);
         if (part == 0) {
-            // 32 threads x 8 columns per row, 8 rows at a time
-            for (int i = w; i < n; i += PREP_THREADS / 32) {
-                if (sm.row_R[i] != nullptr) continue;
-                const int c = lane * 8;
-                if (c < ncols)
-                    *reinterpret_cast<uint4 *>(xs + (size_t)i * p.kdim + col0 + c) =
-                        *reinterpret_cast<const uint4 *>(x + (size_t)sm.perm[i] * p.d_in + col0 + c);
+            // 32 threads x 8 columns per row; each warp handles rows w, w+8, ...
+            // and issues up to 8 row loads before storing any
+            const int c = lane * 8;
+            for (int i0 = w; i0 < n; i0 += 8 * (PREP_THREADS / 32)) {
+                uint4 buf[8];
+                bool live[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * (PREP_THREADS / 32);
+                    live[u] = i < n && c < ncols && sm.row_R[i] == nullptr;
+                    if (live[u]) buf[u] = *reinterpret_cast<const uint4 *>(x + (size_t)sm.perm[i] * p.d_in + col0 + c);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * (PREP_THREADS / 32);
+                    if (live[u]) *reinterpret_cast<uint4 *>(xs + (size_t)i * p.kdim + col0 + c) = buf[u];
+                }
             }
             return;
         }
@@ -290,26 +298,55 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         const int s0 = sm.seg_start[seg], s1 = sm.seg_start[seg + 1];
         const __nv_bfloat16 *Rb = reinterpret_cast<const __nv_bfloat16 *>(sm.row_R[s0]) +
                                   (size_t)(col0 / OFT_BLK) * OFT_BLK * OFT_BLK;
-        const int nvec = (ncols / OFT_BLK) * OFT_BLK * OFT_BLK / 8;
-        for (int e = tid; e < nvec; e += PREP_THREADS) {
-            float v[8];
-            load8(Rb + (size_t)e * 8, v);
+        const int nvec = (ncols / OFT_BLK) * OFT_BLK * OFT_BLK / 8;   // <= 4 per thread
+        {
+            uint4 rbuf[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) (&sm.R[0][0][0])[e * 8 + q] = v[q];
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + u * PREP_THREADS;
+                if (e < nvec) rbuf[u] = *reinterpret_cast<const uint4 *>(Rb + (size_t)e * 8);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + u * PREP_THREADS;
+                if (e < nvec) {
+                    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&rbuf[u]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 f = __bfloat1622float2(h[q]);
+                        (&sm.R[0][0][0])[e * 8 + 2 * q] = f.x;
+                        (&sm.R[0][0][0])[e * 8 + 2 * q + 1] = f.y;
+                    }
+                }
+            }
         }
         // R's 8 blocks of this chunk and up to ROT_ROWS rows of x are staged
         // with 16-byte loads; every thread then produces one column per row
         for (int r0 = s0; r0 < s1; r0 += ROT_ROWS) {
             const int nr = min(ROT_ROWS, s1 - r0);
-            for (int e = tid; e < nr * 32; e += PREP_THREADS) {
-                const int rr = e >> 5, c = (e & 31) * 8;
-                float v[8];
-                if (c < ncols) load8(x + (size_t)sm.perm[r0 + rr] * p.d_in + col0 + c, v);
-                else
+            {
+                uint4 xbuf[2];   // ROT_ROWS * 32 vectors over 256 threads
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = 0.f;
+                for (int u = 0; u < 2; ++u) {
+                    const int e = tid + u * PREP_THREADS, rr = e >> 5, c = (e & 31) * 8;
+                    if (rr < nr && c < ncols)
+                        xbuf[u] = *reinterpret_cast<const uint4 *>(x + (size_t)sm.perm[r0 + rr] * p.d_in + col0 + c);
+                    else
+                        xbuf[u] = make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
-                for (int q = 0; q < 8; ++q) sm.xrows[rr][c + q] = v[q];
+                for (int u = 0; u < 2; ++u) {
+                    const int e = tid + u * PREP_THREADS, rr = e >> 5, c = (e & 31) * 8;
+                    if (rr < nr) {
+                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&xbuf[u]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(h[q]);
+                            sm.xrows[rr][c + 2 * q] = f.x;
+                            sm.xrows[rr][c + 2 * q + 1] = f.y;
+                        }
+                    }
+                }
             }
             __syncthreads();
             if (tid < ncols) {
@@ -361,9 +398,9 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_kernel(const __grid_constan
         __nv_bfloat16 *U = reinterpret_cast<__nv_bfloat16 *>(p.U);
         const int ldu = p.u_ld;
         const Slot *slots = p.slots;
+        (void)slots;
         shrink(x, p.d_in, sm.perm, r0, r1, Arows, nq, sm, [&](int i, int q, float s) {
-            const int a = (int)(sm.skey[i] - (uint32_t)RANK_VERA * A);
-            const float *d = slots[a].vd;
+            const float *d = sm.row_vd[i];
             U[(size_t)i * ldu + q0 + q] = __float2bfloat16_rn(d ? s * d[q0 + q] : 0.f);
         });
     }
