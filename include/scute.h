@@ -206,6 +206,46 @@ scute_status scute_debug_index(scute_ctx *ctx, const int32_t *adapter_ids, int64
                                int32_t *perm, int32_t *aid_sorted, int32_t *seg_start,
                                int32_t *seg_aid, int32_t *counts, void *stream);
 
+/* ---------------------------------------------------------------- token indexing without a context
+ * The article has no counterpart of this call: it is a service of this
+ * library for callers that cannot allocate device memory.  Typical ones: a
+ * batch scheduler or router in a process whose serving engine has already
+ * reserved its device memory pool (most of HBM goes to the KV cache), where a
+ * new allocation fails or takes memory the pool counts on; and code on a
+ * latency-critical path, where cudaMalloc and cudaFree may synchronise the
+ * device.  Such callers still want the adapter segments a batch forms, but
+ * cannot create a context (scute_create allocates its workspaces).
+ *
+ * Runs the kernel scute_debug_index runs, on the CURRENT device and `stream`,
+ * with the same outputs (perm, aid_sorted, seg_start, seg_aid, counts: layout
+ * as for scute_debug_index; all device buffers of the caller), and
+ *   method_of_adapter  HOST int8 [n_adapters]: the scute_method of each
+ *                      adapter id, or -1 where the id names no adapter;
+ *                      copied with cudaMemcpyAsync (pageable memory may be
+ *                      reused when the call returns; pinned memory must stay
+ *                      unchanged until the stream has passed the call);
+ *   flags              device int32 [1] or NULL: nonzero when an id in
+ *                      adapter_ids named no adapter (those tokens become
+ *                      base-only rows, as in scute_linear).
+ * Scratch: a file-scope device array of SCUTE_NOALLOC_SCRATCH_BYTES (the method
+ * table and a status word), located once per device with cudaGetSymbolAddress
+ * on the first call made while that device is current.  That first call may
+ * load the library's module, so make it before any stream capture.  Nothing
+ * is allocated: no cudaMalloc, cudaFree or allocating library routine.
+ * Overlapping calls on one device (other streams, other host threads) share
+ * the array and race; order them on the device.
+ * Errors (nothing is launched): SCUTE_ERR_ARG for a null output, n < 0,
+ * n_adapters < 1 or a method code outside -1..5; SCUTE_ERR_UNSUPPORTED for
+ * n > SCUTE_MAX_TOKENS or n_adapters > SCUTE_NOALLOC_MAX_ADAPTERS (the static
+ * table's size); SCUTE_ERR_NO_DEVICE when the current device is not sm_103;
+ * SCUTE_ERR_CUDA when a CUDA call fails. */
+#define SCUTE_NOALLOC_MAX_ADAPTERS 8192
+#define SCUTE_NOALLOC_SCRATCH_BYTES (256 + SCUTE_NOALLOC_MAX_ADAPTERS)
+scute_status scute_index_tokens_noalloc(const int8_t *method_of_adapter, int32_t n_adapters,
+                                        const int32_t *adapter_ids, int64_t n, int32_t *perm,
+                                        int32_t *aid_sorted, int32_t *seg_start, int32_t *seg_aid,
+                                        int32_t *counts, int32_t *flags, void *stream);
+
 /* ---------------------------------------------------------------- byte model
  * Zero-parameter byte model (article, section "Where is the cheapest place to
  * compute the remaining slots?": added time = extra bytes / memory bandwidth +

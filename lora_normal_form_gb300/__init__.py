@@ -91,6 +91,8 @@ _SIGS = {
     "scute_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
     "scute_debug_index": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64] +
                           [ctypes.c_void_p] * 5 + [ctypes.c_void_p]),
+    "scute_index_tokens_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                  ctypes.c_int64] + [ctypes.c_void_p] * 7),
     "scute_byte_model": (ctypes.c_int, [ctypes.POINTER(BmLayer), ctypes.c_void_p, ctypes.c_int64,
                                         ctypes.POINTER(ByteReport)]),
     "scute_predict_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -210,6 +212,26 @@ def scute_sync_status(ctx) -> int:
 def scute_debug_index(ctx, ids, n, perm, aid_sorted, seg_start, seg_aid, counts, stream=None):
     _check(ctx, load().scute_debug_index(ctx, ptr(ids), n, ptr(perm), ptr(aid_sorted), ptr(seg_start),
                                          ptr(seg_aid), ptr(counts), _stream_handle(stream)))
+
+
+NOALLOC_MAX_ADAPTERS = 8192
+
+
+def scute_index_tokens_noalloc(method_of_adapter, ids, n, perm, aid_sorted, seg_start, seg_aid, counts,
+                               flags=None, stream=None):
+    """Context-free indexing on the current device; ``method_of_adapter`` is a
+    host int8 numpy array (method code per adapter id, -1 = none)."""
+    import numpy as np
+    tab = np.ascontiguousarray(method_of_adapter, dtype=np.int8)
+    code = load().scute_index_tokens_noalloc(ptr(tab), int(tab.size), ptr(ids), n, ptr(perm), ptr(aid_sorted),
+                                             ptr(seg_start), ptr(seg_aid), ptr(counts), ptr(flags),
+                                             _stream_handle(stream))
+    if code != 0:
+        why = {1: "null output, n < 0, no adapters or a method code outside -1..5",
+               8: f"n above {MAX_TOKENS} tokens or more than {NOALLOC_MAX_ADAPTERS} adapters "
+                  "(size of the static method table)",
+               9: "the current device is not sm_103", 6: "a CUDA call failed"}.get(code, "")
+        raise ScuteError(code, why)
 
 
 def scute_byte_model(layer: BmLayer, ids_host, n) -> dict:
