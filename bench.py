@@ -2,19 +2,23 @@
 """Benchmark of the adapted linear layer in normal form on a mixed PEFT batch.
 
 Workload (decode, Llama-3-8B-shaped): one step is one pass of the whole hot
-path -- scute_linear on the six projections q (4096->4096), k, v (4096->1024),
-gate, up (4096->14336) and down (14336->4096) -- for 64 tokens whose ids are
-uniform over 32 adapters, method = id mod 5 (LoRA, DoRA, (IA)^3, VeRA, OFT),
-rank 16, shared VeRA rank 256, OFT blocks of 32.  Inputs are seeded synthetic
-tensors (``workloads.decode_mixed``), resident in device memory before timing.
+path over the six projections q (4096->4096), k, v (4096->1024), gate, up
+(4096->14336) and down (14336->4096) for 64 tokens whose ids are uniform over
+32 adapters, method = id mod 5 (LoRA, DoRA, (IA)^3, VeRA, OFT), rank 16,
+shared VeRA rank 256, OFT blocks of 32.  Inputs are seeded synthetic tensors
+(``workloads.decode_mixed``, one independent input per projection), resident
+in device memory before timing.  The headline step is ONE scute_linear_batch
+call over the six projections (one launch).  Two other groupings of the same
+work are timed beside it: the groups a transformer block's data dependencies
+allow ({q, k, v}, {gate, up}, {down}: three launches) and six separate
+scute_linear calls.
 
 Metric: tokens per second through the adapted layer (one step), plus the
 step's algorithmic HBM GB/s and its overhead against an all-LoRA batch of the
 same size, ids and rank.  Timing: each step is a CUDA graph replay bracketed by
 CUDA events; L2 is flushed (a 512 MiB write) before every step, outside the
-timed interval.  The base-GEMM launches are timed in a second graph of the same
-step whose event records sit on the launching stream around each GEMM launch
-(events there cut the overlap between launches, so the headline graph has none).
+timed interval.  The step kernel is also timed alone, in a second graph whose
+event records sit on the launching stream around the launch.
 
 `--impl reference` times the float64 CPU oracle on the same workload instead
 (a bounded sample per step).  Under torchrun each rank serves its own batch of
@@ -219,7 +223,16 @@ def main():
 
     stream = torch.cuda.Stream(device=dev)
 
+    BLOCK_GROUPS = (("q", "k", "v"), ("gate", "up"), ("down",))
+
     def step(c, o):
+        c.linear_batch([(xs[p], c.layer_ids[p], o[p]) for p in PROJ], ids, "bf16", stream=stream)
+
+    def step_grouped(c, o):
+        for grp in BLOCK_GROUPS:
+            c.linear_batch([(xs[p], c.layer_ids[p], o[p]) for p in grp], ids, "bf16", stream=stream)
+
+    def step_calls(c, o):
         for p in PROJ:
             c.linear(xs[p], ids, c.layer_ids[p], o[p], "bf16", stream=stream)
 
@@ -228,35 +241,35 @@ def main():
         for _ in range(max(1, args.warmup)):
             step(ctx, outs)
             step(ctx_l, outs_l)
+            step_grouped(ctx, outs)
+            step_calls(ctx, outs)
     torch.cuda.synchronize()
     st = ctx.sync_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
-    # the headline graph carries no timing events (an event between two
-    # launches would cut their programmatic-dependent-launch overlap); a second
-    # graph with events around each base-GEMM launch times that kernel alone
+
+    def capture(fn, c, o):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                fn(c, o)
+        return g
+
     n0 = ctx.launch_count()
-    g_mixed = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_mixed, stream=stream):
-            step(ctx, outs)
+    g_mixed = capture(step, ctx, outs)
     launches_per_step = ctx.launch_count() - n0
-    g_lora = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_lora, stream=stream):
-            step(ctx_l, outs_l)
+    g_lora = capture(step, ctx_l, outs_l)
+    g_grouped = capture(step_grouped, ctx, outs)
+    g_calls = capture(step_calls, ctx, outs)
     ctx.timing(True)
     ctx.timing_reset()
-    g_timed = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g_timed, stream=stream):
-            step(ctx, outs)
+    g_timed = capture(step, ctx, outs)
     ctx.timing(False)
 
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
-    def timed(graph, K, read_gemm):
-        t_steps, t_gemm = [], []
+    def timed(graph, K, read_kernel):
+        t_steps, t_kernel = [], []
         for _ in range(K):
             with torch.cuda.stream(stream):
                 flush.fill_(1)
@@ -267,13 +280,13 @@ def main():
                 e1.record(stream)
             e1.synchronize()
             t_steps.append(e0.elapsed_time(e1))
-            if read_gemm:
-                t_gemm.append(ctx.timing_read()[:len(PROJ)])
-        return t_steps, t_gemm
+            if read_kernel:
+                t_kernel.append(ctx.timing_read()[:1])
+        return t_steps, t_kernel
 
     # warm-up replays
-    timed(g_mixed, args.warmup, False)
-    timed(g_lora, args.warmup, False)
+    for g in (g_mixed, g_lora, g_grouped, g_calls):
+        timed(g, args.warmup, False)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -283,8 +296,10 @@ def main():
     clocks = sampler.stop()
     torch.cuda.synchronize()
     t_lora, _ = timed(g_lora, args.steps, False)
+    t_grouped, _ = timed(g_grouped, args.steps, False)
+    t_calls, _ = timed(g_calls, args.steps, False)
     timed(g_timed, args.warmup, False)
-    _, t_gemm = timed(g_timed, min(args.steps, 200), True)
+    _, t_kernel = timed(g_timed, min(args.steps, 200), True)
 
     ms = float(np.mean(t_mixed))
     ms_lora = float(np.mean(t_lora))
@@ -293,22 +308,19 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms, ms_lora = float(tt[0]), float(tt[1])
 
-    # byte model of the step
+    # byte model of the step: the one launch moves every projection's bytes
     bm = {p: ctx.predict_bytes(w.ids, ctx.layer_ids[p], "bf16") for p in PROJ}
     alg_bytes = sum(bm[p]["algorithmic_bytes"] for p in PROJ)
-    gemm_bytes = [dict((k[0], k[1]) for k in bm[p]["kernels"])["base_gemm"] for p in PROJ]
-    gemm_ms = np.array(t_gemm, dtype=np.float64)  # [steps, 6]
-    gemm_avg_ms = float(gemm_ms.mean())
-    gemm_avg_bytes = float(np.mean(gemm_bytes))
+    kernel_ms = float(np.mean(np.array(t_kernel, dtype=np.float64)))
     hbm_peak, _, peak_kind = peaks()
-    achieved = gemm_avg_bytes / (gemm_avg_ms * 1e-3) / 1e9
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
 
     # end to end through the host-buffer entry point (copies inside the timed region)
     h_x = {p: torch.from_numpy(np.ascontiguousarray(w.layer(p).get("x")).view(np.int16))
            .view(torch.bfloat16).pin_memory() for p in PROJ}
     h_ids = torch.from_numpy(w.ids.copy()).pin_memory()
     h_out = {p: torch.empty(w.n, w.layer(p).d_out, dtype=torch.bfloat16).pin_memory() for p in PROJ}
-    h2d = sum(w.n * w.layer(p).d_in * 2 + w.n * 4 for p in PROJ)
+    h2d = sum(w.n * w.layer(p).d_in * 2 for p in PROJ) + w.n * 4
     d2h = sum(w.n * w.layer(p).d_out * 2 for p in PROJ)
     e2e_t = []
     for i in range(args.warmup + min(args.steps, 100)):
@@ -317,8 +329,8 @@ def main():
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for p in PROJ:
-                ctx.linear_host(h_x[p], h_ids, ctx.layer_ids[p], h_out[p], "bf16", stream=stream)
+            ctx.linear_batch_host([(h_x[p], ctx.layer_ids[p], h_out[p]) for p in PROJ], h_ids, "bf16",
+                                  stream=stream)
             e1.record(stream)
         e1.synchronize()
         if i >= args.warmup:
@@ -352,11 +364,12 @@ def main():
         "algorithmic_bytes_per_step": alg_bytes,
         "all_lora_ms_per_step": ms_lora,
         "overhead_vs_all_lora_pct": 100.0 * (ms / ms_lora - 1.0),
-        "roofline": {"kernel": "base_gemm (tcgen05, 6 launches per step)", "bound": "hbm",
+        "roofline": {"kernel": "decode step (tcgen05 + TMA, one persistent launch per step)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_kind": peak_kind, "traffic": None,
-                     "per_projection_ms": {p: float(gemm_ms[:, i].mean()) for i, p in enumerate(PROJ)},
-                     "per_projection_bytes": dict(zip(PROJ, gemm_bytes))},
+                     "peak_kind": peak_kind, "traffic": None, "kernel_ms": kernel_ms,
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "block_groups_ms_per_step": float(np.mean(t_grouped)),
+        "separate_calls_ms_per_step": float(np.mean(t_calls)),
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": int(launches_per_step * args.steps),

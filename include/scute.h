@@ -174,7 +174,9 @@ scute_status scute_unregister_adapter(scute_ctx *ctx, int32_t adapter_id);
  * Steps, all on the device: token indexing (stable grouping by method and
  * adapter id), the OFT input rotation into a workspace copy of x, the base
  * GEMM on tcgen05 tensor cores with the s / b epilogue gathered by adapter,
- * the owned low-rank shrink and expand, and the VeRA shared-pair GEMMs.
+ * the owned low-rank shrink and expand, and the VeRA shared-pair GEMMs.  A
+ * decode batch (bf16 context, n <= 128) runs all of them in one persistent
+ * launch (scute_linear_batch with one call).
  * Returns after enqueueing; x, adapter_ids and out must stay valid until the
  * stream reaches the call. */
 scute_status scute_linear(scute_ctx *ctx, const void *x, const int32_t *adapter_ids, int64_t n,
@@ -187,6 +189,41 @@ scute_status scute_linear(scute_ctx *ctx, const void *x, const int32_t *adapter_
 scute_status scute_linear_host(scute_ctx *ctx, const void *x_host, const int32_t *ids_host,
                                int64_t n, int layer, void *out_host, scute_dtype out_dtype,
                                void *stream);
+
+/* Several layers over the same tokens in one call: for each i < n_calls,
+ * calls[i].out receives the adapted layer calls[i].layer applied to
+ * calls[i].x, all with the one adapter_ids vector (the projections of a
+ * transformer block that read the same batch, such as q, k and v, or gate and
+ * up).  The results are those of n_calls scute_linear calls up to the order of
+ * floating-point sums.
+ *   calls    HOST array of n_calls entries (0..SCUTE_MAX_CALLS); each x and out
+ *            as for scute_linear (device, 16-byte aligned); an out may not
+ *            overlap any call's x or out.  A layer may appear more than once.
+ * A decode batch (bf16 context, n <= 128) runs as ONE persistent cooperative
+ * launch that streams every listed layer's weights once, split over all SMs
+ * in contiguous runs of 64-wide K blocks (section "Where is the cheapest place
+ * to compute the remaining slots?" of the article prices the extra slots in
+ * bytes moved; this launch keeps the one large byte stream, the base weights,
+ * continuous).  Other batches run the calls one after another.  Errors as for
+ * scute_linear; nothing is enqueued when an argument is rejected.  Calls on one
+ * context must be ordered on the device (they share its workspace). */
+#define SCUTE_MAX_CALLS 8
+typedef struct scute_call {
+    const void *x;   /* [n, d_in of layer] */
+    int layer;
+    void *out;       /* [n, d_out of layer] */
+} scute_call;
+scute_status scute_linear_batch(scute_ctx *ctx, const scute_call *calls, int n_calls,
+                                const int32_t *adapter_ids, int64_t n, scute_dtype out_dtype,
+                                void *stream);
+
+/* scute_linear_batch with HOST buffers (every x and out, and adapter_ids, in
+ * host memory): the inputs are copied into context-owned device staging, the
+ * batch runs, the outputs are copied back, all enqueued on `stream`.  The
+ * caller synchronises the stream before reading the outputs. */
+scute_status scute_linear_batch_host(scute_ctx *ctx, const scute_call *calls, int n_calls,
+                                     const int32_t *ids_host, int64_t n, scute_dtype out_dtype,
+                                     void *stream);
 
 /* Synchronise the device and return (then clear) the device status word:
  * SCUTE_OK, SCUTE_ERR_BAD_ADAPTER or SCUTE_ERR_TIMEOUT (timeout wins). */

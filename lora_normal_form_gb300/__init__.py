@@ -69,6 +69,13 @@ class BmLayer(ctypes.Structure):
                 ("max_adapters", ctypes.c_int), ("adapters", ctypes.POINTER(BmAdapter))]
 
 
+class Call(ctypes.Structure):
+    """One entry of a batched call (scute_call)."""
+    _fields_ = [("x", ctypes.c_void_p), ("layer", ctypes.c_int), ("out", ctypes.c_void_p)]
+
+
+MAX_CALLS = 8
+
 _lib: Optional[ctypes.CDLL] = None
 
 _SIGS = {
@@ -88,6 +95,10 @@ _SIGS = {
                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "scute_linear_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
+    "scute_linear_batch": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Call), ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
+    "scute_linear_batch_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Call), ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]),
     "scute_sync_status": (ctypes.c_int, [ctypes.c_void_p]),
     "scute_debug_index": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64] +
                           [ctypes.c_void_p] * 5 + [ctypes.c_void_p]),
@@ -203,6 +214,27 @@ def scute_linear(ctx, x, adapter_ids, n, layer, out, out_dtype, stream=None):
 def scute_linear_host(ctx, x_host, ids_host, n, layer, out_host, out_dtype, stream=None):
     _check(ctx, load().scute_linear_host(ctx, ptr(x_host), ptr(ids_host), n, layer, ptr(out_host),
                                          out_dtype, _stream_handle(stream)))
+
+
+def _calls(calls):
+    arr = (Call * max(1, len(calls)))()
+    for i, (x, layer, out) in enumerate(calls):
+        arr[i].x = ptr(x)
+        arr[i].layer = layer
+        arr[i].out = ptr(out)
+    return arr
+
+
+def scute_linear_batch(ctx, calls, adapter_ids, n, out_dtype, stream=None):
+    """``calls``: sequence of (x, layer, out) with device tensors."""
+    _check(ctx, load().scute_linear_batch(ctx, _calls(calls), len(calls), ptr(adapter_ids), n, out_dtype,
+                                          _stream_handle(stream)))
+
+
+def scute_linear_batch_host(ctx, calls, ids_host, n, out_dtype, stream=None):
+    """``calls``: sequence of (x_host, layer, out_host) with host arrays."""
+    _check(ctx, load().scute_linear_batch_host(ctx, _calls(calls), len(calls), ptr(ids_host), n, out_dtype,
+                                               _stream_handle(stream)))
 
 
 def scute_sync_status(ctx) -> int:

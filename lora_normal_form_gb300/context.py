@@ -4,7 +4,8 @@ from __future__ import annotations
 import numpy as np
 
 from . import (BF16, FP32, METHOD_ID, scute_add_layer, scute_create, scute_debug_index, scute_destroy,
-               scute_launch_count, scute_linear, scute_linear_host, scute_predict_bytes,
+               scute_launch_count, scute_linear, scute_linear_batch, scute_linear_batch_host,
+               scute_linear_host, scute_predict_bytes,
                scute_register_adapter, scute_set_shared, scute_sync_status, scute_timing_enable,
                scute_timing_read, scute_timing_reset, scute_unregister_adapter)
 
@@ -89,6 +90,15 @@ class Context:
     def linear_host(self, x_host, ids_host, layer: int, out_host, out_dtype: str = "bf16", stream=None):
         scute_linear_host(self.handle, x_host, ids_host, int(ids_host.shape[0]), layer, out_host,
                           BF16 if out_dtype == "bf16" else FP32, stream)
+
+    def linear_batch(self, calls, ids, out_dtype: str = "bf16", stream=None, n=None):
+        """``calls``: sequence of (x, layer id, out); every layer sees the same ids."""
+        n = int(ids.shape[0]) if n is None else n
+        scute_linear_batch(self.handle, list(calls), ids, n, BF16 if out_dtype == "bf16" else FP32, stream)
+
+    def linear_batch_host(self, calls, ids_host, out_dtype: str = "bf16", stream=None):
+        scute_linear_batch_host(self.handle, list(calls), ids_host, int(ids_host.shape[0]),
+                                BF16 if out_dtype == "bf16" else FP32, stream)
 
     def sync_status(self) -> int:
         return scute_sync_status(self.handle)

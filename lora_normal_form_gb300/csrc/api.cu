@@ -161,7 +161,13 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               cudaMalloc(&c->d_err, sizeof(int)) == cudaSuccess &&
               cudaMalloc(&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
               cudaMalloc(&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess &&
-              cudaMalloc(&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess;
+              cudaMalloc(&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess &&
+              cudaMalloc(&c->step_v, sizeof(float) * STEP_MAX_CALLS * STEP_MAX_TOKENS * MAX_RANK) == cudaSuccess &&
+              cudaMalloc(&c->step_sync, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
+              cudaMemset(c->step_sync, 0, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
+              cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) ==
+                  cudaSuccess;
+    c->step_bn_max = max_tokens <= 64 ? 64 : 128;
     if (!ok) {
         scute_destroy(c);
         return SCUTE_ERR_OOM;
@@ -183,7 +189,8 @@ void scute_destroy(scute_ctx *c) {
         if (a.storage) cudaFree(a.storage);
     void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
-                    c->st_out, c->st_ids, c->tmp};
+                    c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_v, c->step_part,
+                    c->step_sync, c->step_hx, c->step_hout};
     for (void *p : bufs)
         if (p) cudaFree(p);
     if (c->ev_made)
@@ -223,6 +230,21 @@ scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const
     st = grow(c, &c->xs, &c->xs_cols, (size_t)L.kdim, c->esz, c->max_tokens);
     if (!st) st = grow(c, &c->st_x, &c->st_x_cols, (size_t)d_in, c->esz, c->max_tokens);
     if (!st) st = grow(c, &c->st_out, &c->st_out_cols, (size_t)d_out, 4, c->max_tokens);
+    if (!st && !f32) {
+        // decode-step slots, host-call staging and partial tiles
+        const size_t rows = (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS;
+        st = grow(c, &c->step_xs, &c->step_xs_cols, (size_t)L.kdim, c->esz, rows);
+        if (!st) st = grow(c, &c->step_hx, &c->step_hx_cols, (size_t)d_in, c->esz, rows);
+        if (!st) st = grow(c, &c->step_hout, &c->step_hout_cols, (size_t)d_out, 4, rows);
+        int max_ft = 0;
+        for (const auto &Lr : c->layers)
+            if (Lr.present && (Lr.d_out + 127) / 128 > max_ft) max_ft = (Lr.d_out + 127) / 128;
+        const int G = c->num_sms < STEP_MAX_GRID ? c->num_sms : STEP_MAX_GRID;
+        const size_t slots = (size_t)2 * G + (size_t)STEP_MAX_CALLS * max_ft;
+        void *pp = c->step_part;
+        if (!st) st = grow(c, &pp, &c->step_part_floats, slots * 2 * 128 * c->step_bn_max, 4, 1);
+        c->step_part = reinterpret_cast<float *>(pp);
+    }
     if (st) {
         cudaFree(c->layers[layer].Wt);
         c->layers[layer] = LayerRec();
@@ -267,6 +289,8 @@ scute_status scute_set_shared(scute_ctx *c, int layer, int rank, const void *A_s
     L.rv = rank;
     L.krv = krv;
     st = grow(c, &c->U, &c->u_cols, (size_t)krv, c->esz, c->max_tokens);
+    if (!st && !f32) st = grow(c, &c->step_U, &c->step_u_cols, (size_t)krv, c->esz,
+                               (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS);
     if (st) return st;
     return remap_workspace(c);
 }
@@ -503,6 +527,146 @@ static int max_owned_rank(const scute_ctx *c, int layer) {
     return r;
 }
 
+// One decode step over n_calls layers (bf16 context, n <= STEP_MAX_TOKENS):
+// argument block, stream-K ranges and workspace slots, then one cooperative
+// launch.  Arguments are validated by the callers.
+static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, const int32_t *ids, int nn,
+                                int out_f32, cudaStream_t st) {
+    StepArgs a;
+    memset(&a, 0, sizeof(a));
+    const int G = c->num_sms < STEP_MAX_GRID ? c->num_sms : STEP_MAX_GRID;
+    const int BN = nn <= 64 ? 64 : 128;
+    if (BN > c->step_bn_max) return fail(c, SCUTE_ERR_UNSUPPORTED, "decode workspace sized for fewer tokens");
+    long long blk = 0;
+    int tile = 0, item = 0, rmax = 0;
+    for (int i = 0; i < nc; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        StepCall &k = a.call[i];
+        const bool vera_on = L.rv > 0 && L.n_vera > 0;
+        k.x = calls[i].x;
+        k.xs = reinterpret_cast<uint8_t *>(c->step_xs) + (size_t)i * STEP_MAX_TOKENS * c->step_xs_cols * c->esz;
+        k.U = vera_on ? reinterpret_cast<uint8_t *>(c->step_U) + (size_t)i * STEP_MAX_TOKENS * c->step_u_cols * c->esz
+                      : nullptr;
+        k.v = c->step_v + (size_t)i * STEP_MAX_TOKENS * MAX_RANK;
+        k.out = calls[i].out;
+        k.slots = c->d_slots + (size_t)calls[i].layer * c->max_adapters;
+        k.Wt = L.Wt;
+        k.mapW = L.mapW;
+        if (!encode_map(c, &k.mapXs, k.xs, (uint64_t)L.kdim, (uint64_t)STEP_MAX_TOKENS))
+            return fail(c, SCUTE_ERR_CUDA, "tensor map for the token operand failed");
+        if (vera_on) {
+            k.mapAsh = L.mapAsh;
+            k.mapBsh = L.mapBsh;
+            if (!encode_map(c, &k.mapU, k.U, (uint64_t)L.krv, (uint64_t)STEP_MAX_TOKENS))
+                return fail(c, SCUTE_ERR_CUDA, "tensor map for the VeRA intermediate failed");
+        }
+        k.d_in = L.d_in;
+        k.kdim = L.kdim;
+        k.d_out = L.d_out;
+        k.krv = L.krv;
+        k.rv = L.rv;
+        k.kblocks = (L.kdim + 63) / 64;
+        k.vkb = vera_on ? (L.krv + 63) / 64 : 0;
+        k.n_ft = (L.d_out + 127) / 128;
+        k.n_vt = vera_on ? (L.rv + 127) / 128 : 0;
+        k.lr_rmax = L.n_lr > 0 ? max_owned_rank(c, calls[i].layer) : 0;
+        if (k.lr_rmax > rmax) rmax = k.lr_rmax;
+        k.out_f32 = out_f32;
+        k.copy_items = ((nn + 7) / 8) * ((L.d_in + 2047) / 2048);
+        k.rot_items = (L.n_rot < nn ? L.n_rot : nn) * ((L.d_in + 511) / 512);
+        k.item0 = item;
+        item += k.copy_items + k.rot_items;
+        k.blk0 = blk;
+        blk += (long long)k.n_ft * (k.kblocks + k.vkb);
+        k.tile0 = tile;
+        tile += k.n_ft;
+    }
+    for (int i = 0; i < nc; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        StepCall &k = a.call[i];
+        k.lr_items = k.lr_rmax > 0 ? (L.n_lr < nn ? L.n_lr : nn) * ((k.lr_rmax + 7) / 8) : 0;
+        k.lr_item0 = item;
+        item += k.lr_items;
+    }
+    // VeRA shrink units: the shortest K chunk (a power of two >= 16 blocks)
+    // that gives at most one unit per CTA
+    int ch = 16, units = 0;
+    for (;;) {
+        units = 0;
+        for (int i = 0; i < nc; ++i) units += a.call[i].n_vt * ((a.call[i].kblocks + ch - 1) / ch);
+        if (units <= G) break;
+        ch *= 2;
+    }
+    long long t_vs = 0;
+    int u = 0;
+    std::vector<int> ublk(units > 0 ? units : 1, 0);
+    for (int i = 0; i < nc; ++i) {
+        StepCall &k = a.call[i];
+        k.vs_chunks = (k.kblocks + ch - 1) / ch;
+        k.vs_unit0 = u;
+        for (int vt = 0; vt < k.n_vt; ++vt)
+            for (int cc = 0; cc < k.vs_chunks; ++cc) {
+                const int b0 = cc * ch, b1 = b0 + ch < k.kblocks ? b0 + ch : k.kblocks;
+                ublk[u++] = b1 - b0;
+                t_vs += b1 - b0;
+            }
+    }
+    // stream-K ranges: every CTA gets about (main + VeRA-shrink blocks) / G,
+    // its VeRA unit counted against its share of main blocks
+    const long long W = blk + t_vs;
+    long long vsb = 0;
+    bool mono = true;
+    for (int i = 0; i <= G; ++i) {
+        a.start[i] = (long long)i * W / G - vsb;
+        if (i < units) vsb += ublk[i];
+        if (i > 0 && a.start[i] < a.start[i - 1]) mono = false;
+    }
+    if (!mono || a.start[0] != 0 || a.start[G] != blk)
+        for (int i = 0; i <= G; ++i) a.start[i] = (long long)i * blk / G;
+    a.n_calls = nc;
+    a.n = nn;
+    a.A = c->max_adapters;
+    a.bn = BN;
+    a.grid = G;
+    a.ids = ids;
+    a.method_tab = c->d_method;
+    a.status = c->d_status;
+    a.part = c->step_part;
+    a.sync = c->step_sync;
+    a.t_main = blk;
+    a.w_total = W;
+    a.n_units = units;
+    a.vs_ch = ch;
+    a.n_tiles = tile;
+    a.n_items = item;
+    a.rmax = rmax;
+    int S = 8;
+    while (S > 2 && step_smem_bytes(BN, S, rmax) > (size_t)c->smem_optin) --S;
+    if (step_smem_bytes(BN, S, rmax) > (size_t)c->smem_optin)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "decode step does not fit shared memory");
+    a.stages = S;
+    if ((size_t)(units + tile + G) * 2 * 128 * BN > c->step_part_floats)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "partial-tile workspace too small for this batch");
+    if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
+    const int slot = c->t_next;
+    unsigned ev_flags = cudaEventRecordDefault;
+    if (c->timing) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CU_TRY(c, cudaStreamIsCapturing(st, &cs));
+        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][0], st, ev_flags));
+    }
+    cudaGetLastError();
+    CU_TRY(c, launch_step(a, st));
+    if (c->timing) {
+        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][1], st, ev_flags));
+        c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
+        if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
+    }
+    count_launch(c, 1);
+    return SCUTE_OK;
+}
+
 scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64_t n, int layer, void *out,
                           scute_dtype out_dtype, void *stream) {
     if (!c) return SCUTE_ERR_ARG;
@@ -522,6 +686,10 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     const int nn = (int)n;
     const Slot *slots = c->d_slots + (size_t)layer * c->max_adapters;
     const int out_f32 = out_dtype == SCUTE_FP32 ? 1 : 0;
+    if (!f32 && nn <= STEP_MAX_TOKENS) {
+        const scute_call one = {x, layer, out};
+        return step_launch(c, &one, 1, ids, nn, out_f32, st);
+    }
     int k = 0;
 
     const int lr_rmax = L.n_lr > 0 ? max_owned_rank(c, layer) : 0;
@@ -715,6 +883,82 @@ scute_status scute_linear_host(scute_ctx *c, const void *x_host, const int32_t *
     scute_status s = scute_linear(c, c->st_x, c->st_ids, n, layer, c->st_out, out_dtype, stream);
     if (s) return s;
     CU_TRY(c, cudaMemcpyAsync(out_host, c->st_out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost, st));
+    return SCUTE_OK;
+}
+
+static scute_status check_calls(scute_ctx *c, const scute_call *calls, int n_calls, int64_t n,
+                                scute_dtype out_dtype, bool need_ptrs) {
+    if (n_calls < 0 || n_calls > SCUTE_MAX_CALLS || (n_calls > 0 && !calls))
+        return fail(c, SCUTE_ERR_ARG, "n_calls = %d outside 0..%d", n_calls, SCUTE_MAX_CALLS);
+    if (n < 0 || n > c->max_tokens) return fail(c, SCUTE_ERR_ARG, "n = %lld outside 0..%d", (long long)n, c->max_tokens);
+    if (out_dtype != SCUTE_BF16 && out_dtype != SCUTE_FP32) return fail(c, SCUTE_ERR_DTYPE, "bad out dtype");
+    if (c->dtype == SCUTE_FP32 && out_dtype != SCUTE_FP32)
+        return fail(c, SCUTE_ERR_DTYPE, "an fp32 context writes fp32 output");
+    for (int i = 0; i < n_calls; ++i) {
+        if (!layer_ok(c, calls[i].layer)) return fail(c, SCUTE_ERR_ARG, "call %d: unknown layer %d", i, calls[i].layer);
+        if (need_ptrs && n > 0) {
+            if (!calls[i].x || !calls[i].out) return fail(c, SCUTE_ERR_ARG, "call %d: null argument", i);
+            if ((reinterpret_cast<uintptr_t>(calls[i].x) | reinterpret_cast<uintptr_t>(calls[i].out)) & 15)
+                return fail(c, SCUTE_ERR_ARG, "call %d: x and out must be 16-byte aligned", i);
+        }
+    }
+    return SCUTE_OK;
+}
+
+scute_status scute_linear_batch(scute_ctx *c, const scute_call *calls, int n_calls, const int32_t *ids, int64_t n,
+                                scute_dtype out_dtype, void *stream) {
+    if (!c) return SCUTE_ERR_ARG;
+    scute_status s = check_calls(c, calls, n_calls, n, out_dtype, true);
+    if (s) return s;
+    if (n == 0 || n_calls == 0) return SCUTE_OK;
+    if (!ids) return fail(c, SCUTE_ERR_ARG, "null argument");
+    if (c->dtype == SCUTE_FP32 || n > STEP_MAX_TOKENS) {
+        for (int i = 0; i < n_calls; ++i) {
+            s = scute_linear(c, calls[i].x, ids, n, calls[i].layer, calls[i].out, out_dtype, stream);
+            if (s) return s;
+        }
+        return SCUTE_OK;
+    }
+    DeviceGuard dg(c->device);
+    return step_launch(c, calls, n_calls, ids, (int)n, out_dtype == SCUTE_FP32 ? 1 : 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int n_calls, const int32_t *ids_host,
+                                     int64_t n, scute_dtype out_dtype, void *stream) {
+    if (!c) return SCUTE_ERR_ARG;
+    scute_status s = check_calls(c, calls, n_calls, n, out_dtype, false);
+    if (s) return s;
+    if (n == 0 || n_calls == 0) return SCUTE_OK;
+    if (!ids_host) return fail(c, SCUTE_ERR_ARG, "null argument");
+    for (int i = 0; i < n_calls; ++i)
+        if (!calls[i].x || !calls[i].out) return fail(c, SCUTE_ERR_ARG, "call %d: null argument", i);
+    if (c->dtype == SCUTE_FP32 || n > STEP_MAX_TOKENS) {
+        for (int i = 0; i < n_calls; ++i) {
+            s = scute_linear_host(c, calls[i].x, ids_host, n, calls[i].layer, calls[i].out, out_dtype, stream);
+            if (s) return s;
+        }
+        return SCUTE_OK;
+    }
+    DeviceGuard dg(c->device);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t osz = out_dtype == SCUTE_FP32 ? 4 : 2;
+    scute_call dev[SCUTE_MAX_CALLS];
+    CU_TRY(c, cudaMemcpyAsync(c->st_ids, ids_host, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+    for (int i = 0; i < n_calls; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        dev[i].layer = calls[i].layer;
+        dev[i].x = reinterpret_cast<uint8_t *>(c->step_hx) + (size_t)i * STEP_MAX_TOKENS * c->step_hx_cols * c->esz;
+        dev[i].out = reinterpret_cast<uint8_t *>(c->step_hout) + (size_t)i * STEP_MAX_TOKENS * c->step_hout_cols * 4;
+        CU_TRY(c, cudaMemcpyAsync(const_cast<void *>(dev[i].x), calls[i].x, (size_t)n * L.d_in * c->esz,
+                                  cudaMemcpyHostToDevice, st));
+    }
+    s = step_launch(c, dev, n_calls, c->st_ids, (int)n, out_dtype == SCUTE_FP32 ? 1 : 0, st);
+    if (s) return s;
+    for (int i = 0; i < n_calls; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        CU_TRY(c, cudaMemcpyAsync(calls[i].out, dev[i].out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost, st));
+    }
     return SCUTE_OK;
 }
 

@@ -74,6 +74,21 @@ struct scute_ctx {
     size_t st_x_cols = 0, st_out_cols = 0;
     void *tmp = nullptr;
     size_t tmp_bytes = 0;
+    // decode-step workspace: STEP_MAX_CALLS slots of STEP_MAX_TOKENS rows each
+    void *step_xs = nullptr;     // token operands, slot row pitch step_xs_cols elements
+    size_t step_xs_cols = 0;
+    void *step_U = nullptr;      // VeRA intermediates
+    size_t step_u_cols = 0;
+    float *step_v = nullptr;     // owned low-rank intermediates [slot][128][MAX_RANK]
+    float *step_part = nullptr;  // partial tiles
+    size_t step_part_floats = 0;
+    int *step_sync = nullptr;    // counters (STEP_SYNC_INTS, zero between launches)
+    void *step_hx = nullptr;     // host-call staging of the inputs / outputs
+    size_t step_hx_cols = 0;
+    void *step_hout = nullptr;
+    size_t step_hout_cols = 0;
+    int step_bn_max = 64;
+    int smem_optin = 0;
     PFN_encodeTiled encode = nullptr;
     int64_t launches = 0;
     bool timing = false;

@@ -165,6 +165,81 @@ struct PrepArgs {
 size_t prep_smem_bytes();
 cudaError_t launch_prep(const PrepArgs &p, int grid, cudaStream_t st, bool pdl);
 
+// ---------------------------------------------------------------- decode step
+// Every projection of one batched call (up to STEP_MAX_CALLS layers over the
+// same n <= 128 tokens) in one persistent cooperative launch: the prologue
+// work (gather / OFT rotation of the token operand, owned low-rank shrink) on
+// the epilogue warps, the VeRA shared shrink as tcgen05 K-chunks, and every
+// layer's base GEMM tiles with the VeRA expand K blocks, split over the CTAs
+// by contiguous ranges of 64-wide K blocks (stream-K), partial tiles summed
+// by the last CTA to finish each tile.
+constexpr int STEP_MAX_CALLS = 8;
+constexpr int STEP_MAX_TOKENS = 128;
+constexpr int STEP_MAX_GRID = 190;
+constexpr int STEP_MAX_VTILES = 8;     // VeRA shrink tiles per call (shared rank <= 1024)
+
+// Layout of the step's int counter array (device, zero between launches).
+enum : int {
+    SY_XS = 0,           // [call] prologue items that wrote the call's token operand
+    SY_LR = 8,           // [call] low-rank shrink items done
+    SY_U = 16,           // [call] VeRA shrink tiles finished
+    SY_EXIT = 24,        // CTAs that left
+    SY_ABORT = 25,       // a CTA gave up a wait
+    SY_VTILE = 32,       // [call * 8 + tile] arrivals at a VeRA shrink tile
+    SY_TILE = 96         // [main tile] arrivals
+};
+constexpr int STEP_SYNC_INTS = 1 << 16;
+
+struct StepCall {
+    CUtensorMap mapW;          // W^T [d_out][kdim]
+    CUtensorMap mapXs;         // token operand [128][kdim]
+    CUtensorMap mapAsh;        // A_sh^T [rv][kdim]
+    CUtensorMap mapBsh;        // B_sh^T [d_out][krv]
+    CUtensorMap mapU;          // VeRA intermediate [128][krv]
+    const void *x;             // [n][d_in] caller input
+    void *xs;                  // [128][kdim]
+    void *U;                   // [128][krv]
+    float *v;                  // [128][MAX_RANK]
+    void *out;                 // [n][d_out]
+    const Slot *slots;         // the layer's slot row
+    const void *Wt;            // W^T base (L2 prefetch)
+    long long blk0;            // first main block (stream-K order)
+    int d_in, kdim, d_out, krv, rv;
+    int kblocks;               // 64-wide K blocks of the base GEMM
+    int vkb;                   // VeRA expand K blocks per main tile (0: none)
+    int n_ft;                  // main tiles (128 features each)
+    int n_vt;                  // VeRA shrink tiles (128 shared ranks each; 0: none)
+    int vs_chunks;             // VeRA shrink units per VeRA tile
+    int vs_unit0;              // first VeRA shrink unit
+    int tile0;                 // first main tile id
+    int lr_rmax;               // largest owned rank (0: no low-rank shrink)
+    int out_f32;
+    int copy_items, rot_items, lr_items;
+    int item0;                 // first gather / rotate item
+    int lr_item0;              // first low-rank item
+};
+
+struct StepArgs {
+    StepCall call[STEP_MAX_CALLS];
+    int n_calls, n, A, bn, stages, grid;
+    const int32_t *ids;
+    const int8_t *method_tab;
+    int *status;
+    float *part;               // partial tiles: slot * 2 planes * 128 * bn floats
+    int *sync;
+    long long t_main;          // main K blocks over all calls
+    long long w_total;         // main + VeRA shrink K blocks
+    int n_units;               // VeRA shrink units (<= grid)
+    int vs_ch;                 // K blocks per VeRA shrink unit
+    int n_tiles;               // main tiles over all calls
+    int n_items;               // prologue items over all calls
+    int rmax;                  // largest lr_rmax (shared-memory v rows)
+    long long start[STEP_MAX_GRID + 1];   // main-block range of each CTA: [start[i], start[i+1])
+};
+
+size_t step_smem_bytes(int bn, int stages, int rmax);
+cudaError_t launch_step(const StepArgs &a, cudaStream_t st);
+
 // ---------------------------------------------------------------- other kernels
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,

@@ -95,17 +95,6 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
     }
 }
 
-__device__ __forceinline__ void store_elem(void *out, int f32, size_t idx, float v, bool add) {
-    if (f32) {
-        float *o = reinterpret_cast<float *>(out) + idx;
-        *o = add ? (*o + v) : v;
-    } else {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out) + idx;
-        const float prev = add ? __bfloat162float(*o) : 0.f;
-        *o = __float2bfloat16_rn(prev + v);
-    }
-}
-
 // Per-token context of the epilogue: which output row and which live slots.
 struct TokMeta {
     long long out_row;     // token index (output row) or U row
@@ -360,17 +349,6 @@ __device__ __forceinline__ void emit8(const GemmArgs &g, const TokMeta &m, const
         for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
         *o = pk;
     }
-}
-
-// Plain load from a cluster peer's shared memory.  No memory clobber: the
-// cluster barriers around the reduction order it, and loads without one can be
-// issued back to back.
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }

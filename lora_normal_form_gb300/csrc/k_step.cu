@@ -1,0 +1,1134 @@
+// Decode step: every projection of one batched call in one persistent launch.
+//
+// The adapted layer of the article "Scute: Exact Batched Serving for PEFT
+// Adapters Beyond LoRA" (paper-daily.com), section "The big picture: six extra
+// slots in the LoRA computation":
+//     F_a(x) = ((x R_a) W) * s_a + b_a + (x A'_a) B'_a + (((x A_sh) * d_a) B_sh) * e_a
+// with the slots already folded at load (section "Which slots can be merged at
+// load?").  For a decode batch (n <= 128 tokens) the work of every layer of
+// the call is one HBM stream of the base weights, so the launch is organised
+// around that stream (section "Where is the cheapest place to compute the
+// remaining slots?": the extra work is priced in bytes moved):
+//
+//   * prologue, on the epilogue warps of every CTA while the weights start to
+//     stream: the ids are ordered by (method, adapter) in shared memory; the
+//     token operand x' (x R_a for rotated rows, x otherwise, kept in token
+//     order) is written per layer; the owned low-rank shrink v = x A'_a runs
+//     per adapter segment;
+//   * VeRA shared shrink U = (x' A_sh) * d_a on tcgen05, cut into short
+//     K-chunks that are the first work of many CTAs, so that U is ready long
+//     before the base tiles reach their VeRA blocks;
+//   * base tiles D[128 features x BN tokens] = W^T x'^T on tcgen05 (TMA-fed,
+//     TMEM accumulators), each tile's K loop followed by the VeRA expand
+//     U B_sh as extra K blocks into a second accumulator; the 64-wide K blocks
+//     of all tiles of all layers are split over the CTAs in contiguous ranges
+//     (stream-K), and the CTA that finishes a tile last sums the other CTAs'
+//     partial tiles and applies s, b, v B' and the VeRA e in its epilogue.
+//
+// Waits between CTAs (token operand written, U written, v written) are
+// counters in global memory, read with acquire loads and bounded in time; the
+// launch is cooperative, so every CTA is resident.  Every mbarrier wait is
+// bounded too; on expiry a CTA records STATUS_TIMEOUT, raises the launch-wide
+// abort flag, drains what it issued, frees TMEM and returns.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 2..9 run the prologue and then the epilogues.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace scute {
+
+namespace {
+
+constexpr int THREADS = 320;
+constexpr int EPI_THREADS = 256;              // warps 2..9
+constexpr int EPI_WARPS = EPI_THREADS / 32;
+constexpr int TILE_M = 128;
+constexpr int BOX_ROWS = 64;
+constexpr int BOX_BYTES = BOX_ROWS * 128;
+constexpr int P_BYTES = TILE_M * 128;
+constexpr int MAX_STAGES = 8;
+constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait
+constexpr int RED = TILE_M + 4;               // token-row stride of a transposed chunk (floats)
+constexpr int XB_FLOATS = 2 * 32 * RED;       // main + VeRA chunk of 32 tokens
+constexpr int PF_AHEAD = 24;                  // K blocks of W asked from L2 at start
+constexpr int PF_CHUNK = 24;                  // K blocks per L2 request run
+constexpr int NTOK = STEP_MAX_TOKENS;
+constexpr int NCALL = STEP_MAX_CALLS;
+constexpr int LR_Q = 8;                       // ranks per low-rank shrink item
+constexpr int LR_ROWS = 2;                    // rows per pass of the shrink
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// f32 accumulator, bf16 A and B, both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct Ctrl {
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;          // this CTA gave up a wait
+    int flag;           // broadcast among the epilogue warps
+    int meta_call;      // call whose token metadata is staged (-1: none)
+    int v_call;         // call whose low-rank rows are staged
+    int n_seg;
+    int bad;
+    int warp_tot[EPI_WARPS];
+    int n_oft[NCALL], n_lrs[NCALL];
+};
+constexpr int CTRL_BYTES = 512;
+static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
+
+// Per-token slots of one layer, as the epilogue uses them.
+struct TokMeta {
+    const float *s, *b, *ve, *vd;
+    const __nv_bfloat16 *B;
+    int rank;    // owned rank applied in the epilogue (0: none)
+    int vera;    // the token takes the VeRA expand
+};
+
+struct Fixed {
+    long long start[STEP_MAX_GRID + 1];   // stream-K range of each CTA
+    uint32_t key[NTOK], skey[NTOK];
+    int perm[NTOK];                       // sorted row -> token
+    int tok_aid[NTOK];                    // token -> adapter (-1: base only)
+    int tok_seg[NTOK];                    // token -> segment
+    int seg_start[NTOK + 1], seg_aid[NTOK];
+    const __nv_bfloat16 *segR[NCALL][NTOK];   // per call: rotation of each segment (null: none)
+    const __nv_bfloat16 *segA[NCALL][NTOK];   // per call: owned A' of each segment (null: none)
+    uint8_t segRank[NCALL][NTOK];
+    uint8_t oft_list[NCALL][NTOK];            // per call: segments with a rotation
+    uint8_t lr_list[NCALL][NTOK];             // per call: segments with an owned term
+    uint32_t oft_mask[NCALL][NTOK / 32];      // per call: tokens whose row is rotated
+    TokMeta tmeta[NTOK];
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        v[2 * e] = f.x;
+        v[2 * e + 1] = f.y;
+    }
+}
+
+// Bounded wait on an mbarrier phase; gives up when the time limit passes or
+// when this CTA or another one has given up.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                      const int *gabort, bool honour_abort = true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (honour_abort && (*abort_flag || *reinterpret_cast<const volatile int *>(gabort))) {
+            *abort_flag = 1;
+            return false;
+        }
+        if (ptx::globaltimer() - t0 > WAIT_NS) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait until the counter at p reaches target (acquire).
+__device__ __noinline__ bool wait_count(const int *p, int target, volatile int *abort_flag, const int *gabort) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire(p) >= target) return true;
+        if (*abort_flag || *reinterpret_cast<const volatile int *>(gabort)) {
+            *abort_flag = 1;
+            return false;
+        }
+        if (ptx::globaltimer() - t0 > WAIT_NS) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Non-blocking look at a counter (acquire).
+__device__ __forceinline__ bool count_reached(const int *p, int target) { return ld_acquire(p) >= target; }
+
+// ---------------------------------------------------------------- schedule
+struct ULoc {      // one VeRA shrink unit: K blocks [kb0, kb1) of VeRA tile vt of call c
+    int c, vt, kb0, kb1;
+};
+__device__ __forceinline__ ULoc ulocate(const StepArgs &a, int u) {
+    int c = 0;
+    while (c + 1 < a.n_calls && a.call[c + 1].vs_unit0 <= u) ++c;
+    const StepCall &k = a.call[c];
+    const int l = u - k.vs_unit0;
+    ULoc r;
+    r.c = c;
+    r.vt = l / k.vs_chunks;
+    const int ch = l - r.vt * k.vs_chunks;
+    r.kb0 = ch * a.vs_ch;
+    r.kb1 = min(k.kblocks, r.kb0 + a.vs_ch);
+    return r;
+}
+
+struct MLoc {      // the main tile that holds stream-K block b
+    int c, tile, kb, nkb;
+    long long tb0;
+};
+__device__ __forceinline__ MLoc mlocate(const StepArgs &a, long long b) {
+    int c = 0;
+    while (c + 1 < a.n_calls && a.call[c + 1].blk0 <= b) ++c;
+    const StepCall &k = a.call[c];
+    const int mpt = k.kblocks + k.vkb;
+    const long long l = b - k.blk0;
+    MLoc r;
+    r.c = c;
+    r.tile = (int)(l / mpt);
+    r.kb = (int)(l - (long long)r.tile * mpt);
+    r.nkb = mpt;
+    r.tb0 = k.blk0 + (long long)r.tile * mpt;
+    return r;
+}
+
+// The CTA whose range holds main block b.
+__device__ __forceinline__ int owner(const Fixed &fx, int G, long long b) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (fx.start[mid] <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------- epilogue pieces
+// Write this warp's half of a 128-row accumulator plane (TMEM columns
+// [tcol, tcol + BN)) as rows of the partial tile [token][128] fp32 (tokens < n).
+__device__ __forceinline__ void publish(uint32_t tcol, float *dst, int n, int BN, int row, int half) {
+    const int per = BN / 64;   // 32-column chunks per warp
+    for (int c = half * per; c < (half + 1) * per; ++c) {
+        if (c * 32 >= n) break;   // uniform across the warp
+        float v[32];
+        ptx::tmem_ld32(tcol + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (c * 32 + k < n) dst[(size_t)(c * 32 + k) * TILE_M + row] = v[k];
+    }
+}
+
+// Count this CTA's arrival at a shared tile; true for the last of n_ctr.
+__device__ __forceinline__ bool arrive(int *cnt, int n_ctr, Ctrl *ctrl, int et) {
+    __threadfence();
+    epi_bar();
+    if (et == 0) {
+        const int old = atomicAdd(cnt, 1);
+        const int last = old == n_ctr - 1;
+        if (last) atomicExch(cnt, 0);
+        ctrl->flag = last;
+    }
+    epi_bar();
+    const bool last = ctrl->flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// Stage the per-token slots of call c (all epilogue threads).
+__device__ void stage_meta(const StepArgs &a, int c, Fixed &fx, Ctrl *ctrl, int et) {
+    if (ctrl->meta_call == c) return;
+    epi_bar();
+    const StepCall &k = a.call[c];
+    for (int t = et; t < a.n; t += EPI_THREADS) {
+        TokMeta m;
+        m.s = m.b = m.ve = m.vd = nullptr;
+        m.B = nullptr;
+        m.rank = 0;
+        m.vera = 0;
+        const int aid = fx.tok_aid[t];
+        if (aid >= 0) {
+            const Slot &sl = k.slots[aid];
+            m.s = sl.s;
+            m.b = sl.b;
+            if (k.lr_rmax > 0 && sl.B && sl.rank > 0) {
+                m.B = reinterpret_cast<const __nv_bfloat16 *>(sl.B);
+                m.rank = sl.rank;
+            }
+            m.vd = sl.vd;
+            if (k.vkb > 0 && sl.vd) {
+                m.vera = 1;
+                m.ve = sl.ve;
+            }
+        }
+        fx.tmeta[t] = m;
+    }
+    if (et == 0) ctrl->meta_call = c;
+    epi_bar();
+}
+
+__device__ __forceinline__ void ld_vec8(const float *p, bool ok, float fill, float (&v)[8]) {
+    if (ok) {
+        const float4 a0 = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 a1 = __ldg(reinterpret_cast<const float4 *>(p + 4));
+        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w; v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = fill;
+    }
+}
+
+// Add the partial rows [t][f0, f0+8) of one plane of a partial slot.
+__device__ __forceinline__ void add_part(const float *src, float (&acc)[8]) {
+    const float4 p0 = __ldcg(reinterpret_cast<const float4 *>(src));
+    const float4 p1 = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+    acc[0] += p0.x; acc[1] += p0.y; acc[2] += p0.z; acc[3] += p0.w;
+    acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
+}
+
+// Two output items (token t[p], features [j0[p], j0[p]+8)) of one layer:
+// y = acc * s + b + v B'[:, j0:j0+8] + vacc * e, every independent load of
+// both items issued before any of them is used.
+__device__ __forceinline__ void emit_pair(const StepCall &k, const TokMeta *const (&m)[2],
+                                          const float *const (&vrow)[2], const int (&t)[2], const int (&j0)[2],
+                                          const bool (&live)[2], float (&acc)[2][8], const float (&vacc)[2][8]) {
+    float y[2][8];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        float s8[8], b8[8], e8[8];
+        ld_vec8(m[p]->s + j0[p], live[p] && m[p]->s, 1.f, s8);
+        ld_vec8(m[p]->b + j0[p], live[p] && m[p]->b, 0.f, b8);
+        ld_vec8(m[p]->ve + j0[p], live[p] && m[p]->ve, 1.f, e8);
+        const float vs = m[p]->vera ? 1.f : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y[p][q] = fmaf(acc[p][q], s8[q], b8[q]) + vs * vacc[p][q] * e8[q];
+    }
+    const int r0 = live[0] ? m[0]->rank : 0, r1 = live[1] ? m[1]->rank : 0;
+    const int rmax = r0 > r1 ? r0 : r1;
+    for (int q0 = 0; q0 < rmax; q0 += 8) {
+        uint4 bq[2][8];
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q0 + q < (p ? r1 : r0))
+                    bq[p][q] = __ldg(reinterpret_cast<const uint4 *>(m[p]->B + j0[p] + (size_t)(q0 + q) * k.d_out));
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q0 + q < (p ? r1 : r0)) {
+                    const float vq = vrow[p][q0 + q];
+                    float bf[8];
+                    unpack8(bq[p][q], bf);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[p][e] = fmaf(vq, bf[e], y[p][e]);
+                }
+            }
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        if (!live[p]) continue;
+        if (k.out_f32) {
+            float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(k.out) + (size_t)t[p] * k.d_out + j0[p]);
+            o[0] = make_float4(y[p][0], y[p][1], y[p][2], y[p][3]);
+            o[1] = make_float4(y[p][4], y[p][5], y[p][6], y[p][7]);
+        } else {
+            uint4 pk;
+            __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[p][2 * e], y[p][2 * e + 1]);
+            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(k.out) + (size_t)t[p] * k.d_out + j0[p]) = pk;
+        }
+    }
+}
+
+// x_i A_rows^T for up to LR_Q rows of A (each [d_in], bf16) and the sorted
+// rows [r0, r1) (tokens perm[r]); emit(token, q, value) once per (row, q).
+// Each of the 256 threads covers 8 consecutive k per pass; a warp reduces its
+// 16 partial sums (2 rows x 8 ranks) with a transposing butterfly, and the 8
+// warps' sums are added in a fixed order.
+template <typename Emit>
+__device__ void shrink256(const __nv_bfloat16 *x, int d_in, const int *perm, int r0, int r1,
+                          const __nv_bfloat16 *Arows, int nq, float *red, int et, Emit emit) {
+    const int lane = et & 31, w = et >> 5;
+    for (int rc = r0; rc < r1; rc += LR_ROWS) {
+        const int nr = min(LR_ROWS, r1 - rc);
+        float v[LR_ROWS * LR_Q];
+#pragma unroll
+        for (int i = 0; i < LR_ROWS * LR_Q; ++i) v[i] = 0.f;
+        const __nv_bfloat16 *xr[LR_ROWS];
+#pragma unroll
+        for (int r = 0; r < LR_ROWS; ++r) xr[r] = x + (size_t)perm[rc + (r < nr ? r : 0)] * d_in;
+#pragma unroll 2
+        for (int kk = et * 8; kk < d_in; kk += EPI_THREADS * 8) {
+            uint4 au[LR_Q], xu[LR_ROWS];
+#pragma unroll
+            for (int q = 0; q < LR_Q; ++q)
+                au[q] = q < nq ? *reinterpret_cast<const uint4 *>(Arows + (size_t)q * d_in + kk) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int r = 0; r < LR_ROWS; ++r)
+                xu[r] = r < nr ? *reinterpret_cast<const uint4 *>(xr[r] + kk) : make_uint4(0u, 0u, 0u, 0u);
+            float xv[LR_ROWS][8];
+#pragma unroll
+            for (int r = 0; r < LR_ROWS; ++r) unpack8(xu[r], xv[r]);
+#pragma unroll
+            for (int q = 0; q < LR_Q; ++q) {
+                float av[8];
+                unpack8(au[q], av);
+#pragma unroll
+                for (int r = 0; r < LR_ROWS; ++r)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[r * LR_Q + q] = fmaf(xv[r][e], av[e], v[r * LR_Q + q]);
+            }
+        }
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            const int o = 16 >> st, half = 8 >> st;
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        if ((lane & 1) == 0) red[w * 16 + (lane >> 1)] = v[0];
+        epi_bar();
+        if (et < 16) {
+            const int r = et / LR_Q, q = et % LR_Q;
+            float s = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < EPI_WARPS; ++ww) s += red[ww * 16 + et];
+            if (r < nr && q < nq) emit(perm[rc + r], q, s);
+        }
+        epi_bar();
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant__ StepArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+    uint8_t *sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const int BN = a.bn, S = a.stages, G = a.grid, me = (int)blockIdx.x;
+    const int STAGE = P_BYTES + BN * 128;
+    const uint32_t NCOLS = 4u * (uint32_t)BN;
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(sbase + S * STAGE);
+    Fixed &fx = *reinterpret_cast<Fixed *>(sbase + S * STAGE + CTRL_BYTES);
+    float *xb = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&fx) + sizeof(Fixed));
+    float *vsm = xb + XB_FLOATS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort_flag = &ctrl->abort;
+    int *sync = a.sync;
+    const int *gabort = sync + SY_ABORT;
+    const size_t SLOT = (size_t)2 * TILE_M * BN;   // floats per partial slot
+
+    // ---- set-up
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctrl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&ctrl->tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctrl->tempty[b]), EPI_WARPS);
+        }
+        ptx::mbar_init(ptx::smem_u32(&ctrl->drain), 1);
+        ctrl->abort = 0;
+        ctrl->meta_call = ctrl->v_call = -1;
+        ctrl->bad = 0;
+        ptx::fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i <= G; i += THREADS) fx.start[i] = a.start[i];
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&ctrl->tmem_base), NCOLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const long long ms = fx.start[me], mend = fx.start[me + 1];
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            for (int c = 0; c < a.n_calls; ++c) {
+                ptx::prefetch_tmap(&a.call[c].mapW);
+                ptx::prefetch_tmap(&a.call[c].mapXs);
+            }
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            unsigned xs_ok = 0, u_ok = 0;
+            bool ok = true;
+            // stages whose weight boxes are issued but whose token-operand
+            // boxes wait until the prologue has written that call's x'
+            int pend_n = 0, pend_head = 0;
+            uint32_t pend_sQ[MAX_STAGES], pend_fb[MAX_STAGES];
+            int pend_kc[MAX_STAGES], pend_c[MAX_STAGES];
+            auto issue_q = [&](uint32_t sQ, uint32_t fb, const CUtensorMap *mq, int kc) {
+                for (int j = 0; j < BN / BOX_ROWS; ++j) ptx::tma_load_2d(sQ + j * BOX_BYTES, mq, kc, j * BOX_ROWS, fb);
+            };
+            auto xs_ready = [&](int c, bool block) -> bool {
+                if ((xs_ok >> c) & 1u) return true;
+                const StepCall &k = a.call[c];
+                const int target = k.copy_items + k.rot_items;
+                if (block) {
+                    if (!wait_count(sync + SY_XS + c, target, abort_flag, gabort)) return false;
+                } else if (!count_reached(sync + SY_XS + c, target)) {
+                    return false;
+                }
+                fence_proxy_async_global();
+                xs_ok |= 1u << c;
+                return true;
+            };
+            // issue pending token boxes in order; with block, wait for them
+            auto flush = [&](bool block) -> bool {
+                while (pend_n > 0) {
+                    const int i = pend_head;
+                    if (!xs_ready(pend_c[i], block)) {
+                        if (!block) return true;
+                        // gave up: issue them anyway (in bounds) so that every
+                        // barrier completes and the copies can be drained
+                        while (pend_n > 0) {
+                            const int j = pend_head;
+                            issue_q(pend_sQ[j], pend_fb[j], &a.call[pend_c[j]].mapXs, pend_kc[j]);
+                            pend_head = (pend_head + 1) % MAX_STAGES;
+                            --pend_n;
+                        }
+                        return false;
+                    }
+                    issue_q(pend_sQ[i], pend_fb[i], &a.call[pend_c[i]].mapXs, pend_kc[i]);
+                    pend_head = (pend_head + 1) % MAX_STAGES;
+                    --pend_n;
+                }
+                return true;
+            };
+            // one stage: P rows [prow, prow + 128) and the token operand, both at K offset kc
+            auto issue = [&](const CUtensorMap *mp, int prow, const CUtensorMap *mq, int kc, int c, bool xs_dep) -> bool {
+                if (pend_n == S && !flush(true)) return false;
+                if (!wait_bar(ptx::smem_u32(&ctrl->empty[stage]), phase ^ 1, abort_flag, gabort)) return false;
+                const uint32_t fb = ptx::smem_u32(&ctrl->full[stage]);
+                const uint32_t sP = ptx::smem_u32(sbase + stage * STAGE);
+                const uint32_t sQ = sP + P_BYTES;
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
+                ptx::tma_load_2d(sP, mp, kc, prow, fb);
+                ptx::tma_load_2d(sP + BOX_BYTES, mp, kc, prow + BOX_ROWS, fb);
+                if (!xs_dep) {
+                    issue_q(sQ, fb, mq, kc);
+                } else {
+                    flush(false);
+                    if (pend_n == 0 && xs_ready(c, false)) {
+                        issue_q(sQ, fb, mq, kc);
+                    } else {
+                        const int i = (pend_head + pend_n) % MAX_STAGES;
+                        pend_sQ[i] = sQ;
+                        pend_fb[i] = fb;
+                        pend_kc[i] = kc;
+                        pend_c[i] = c;
+                        ++pend_n;
+                    }
+                }
+                ++issued;
+                if (++stage == S) { stage = 0; phase ^= 1; }
+                return true;
+            };
+            for (int u = me; ok && u < a.n_units; u += G) {
+                const ULoc U = ulocate(a, u);
+                const StepCall &k = a.call[U.c];
+                for (int kb = U.kb0; ok && kb < U.kb1; ++kb)
+                    ok = issue(&k.mapAsh, U.vt * TILE_M, &k.mapXs, kb * 64, U.c, true);
+            }
+            for (long long b = ms; ok && b < mend;) {
+                const MLoc L = mlocate(a, b);
+                const StepCall &k = a.call[L.c];
+                const long long se = min(mend, L.tb0 + L.nkb);
+                for (int kb = L.kb; ok && b < se; ++b, ++kb) {
+                    const bool vb = kb >= k.kblocks;
+                    if (vb && !((u_ok >> L.c) & 1u)) {
+                        // this CTA's own pending stages may be what U waits for
+                        ok = flush(true) && wait_count(sync + SY_U + L.c, k.n_vt, abort_flag, gabort);
+                        if (!ok) break;
+                        fence_proxy_async_global();
+                        u_ok |= 1u << L.c;
+                    }
+                    ok = vb ? issue(&k.mapBsh, L.tile * TILE_M, &k.mapU, (kb - k.kblocks) * 64, L.c, false)
+                            : issue(&k.mapW, L.tile * TILE_M, &k.mapXs, kb * 64, L.c, true);
+                }
+            }
+            flush(true);
+            // every issued copy must have landed before the CTA may exit
+            const int m_max = issued < S ? (int)issued : S;
+            for (int m = 1; m <= m_max; ++m) {
+                const int s = (stage - m + S) % S;
+                const uint32_t ph = (s < stage) ? phase : (phase ^ 1);
+                wait_bar(ptx::smem_u32(&ctrl->full[s]), ph, abort_flag, gabort, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            const uint32_t IDESC = idesc_bf16(TILE_M, BN);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, bph = 0;
+            bool ok = true;
+            // one segment: nblk K blocks starting at kb_first; blocks at or
+            // beyond kmain go to the second (VeRA) accumulator of the buffer
+            auto segment = [&](int nblk, int kb_first, int kmain) -> bool {
+                if (!wait_bar(ptx::smem_u32(&ctrl->tempty[buf]), bph ^ 1, abort_flag, gabort)) return false;
+                ptx::tc_fence_after();
+                bool fm = true, fv = true;
+                for (int i = 0; i < nblk; ++i) {
+                    const bool vb = kb_first + i >= kmain;
+                    if (!wait_bar(ptx::smem_u32(&ctrl->full[stage]), phase, abort_flag, gabort)) return false;
+                    ptx::tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(buf * 2 * BN + (vb ? BN : 0));
+                    const uint32_t sP = ptx::smem_u32(sbase + stage * STAGE);
+                    const uint64_t da = sw128_desc(sP), db = sw128_desc(sP + P_BYTES);
+                    const bool first = vb ? fv : fm;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(d, da + 2 * kk, db + 2 * kk, IDESC, (kk > 0 || !first) ? 1u : 0u);
+                    if (vb) fv = false;
+                    else fm = false;
+                    ptx::mma_commit(ptx::smem_u32(&ctrl->empty[stage]));
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[buf]));
+                if (++buf == 2) { buf = 0; bph ^= 1; }
+                return true;
+            };
+            for (int u = me; ok && u < a.n_units; u += G) {
+                const ULoc U = ulocate(a, u);
+                ok = segment(U.kb1 - U.kb0, U.kb0, 1 << 30);
+            }
+            for (long long b = ms; ok && b < mend;) {
+                const MLoc L = mlocate(a, b);
+                const long long se = min(mend, L.tb0 + L.nkb);
+                ok = segment((int)(se - b), L.kb, a.call[L.c].kblocks);
+                b = se;
+            }
+            // all MMAs issued here must finish before TMEM is released
+            ptx::mma_commit(ptx::smem_u32(&ctrl->drain));
+            wait_bar(ptx::smem_u32(&ctrl->drain), 0, abort_flag, gabort, false);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= prologue, then epilogues
+        const int et = threadIdx.x - 64;   // 0..255
+        const int ew = et >> 5;            // epilogue warp 0..7
+        const int q4 = warp & 3;           // TMEM lane quadrant this warp may read
+        const int half = ew >> 2;          // which half of the columns (or planes) it drains
+        const int row = q4 * 32 + lane;
+        const int n = a.n;
+        const uint32_t A = (uint32_t)a.A;
+
+        // ---- order the ids: key = (method, adapter), ties in token order
+        {
+            const uint32_t base_key = (uint32_t)RANK_BASE * A;
+            if (et < n) {
+                const int id = a.ids[et];
+                int m = -1;
+                if (id >= 0 && id < a.A) m = a.method_tab[id];
+                if (m < 0 && id != -1) ctrl->bad = 1;
+                fx.tok_aid[et] = m >= 0 ? id : -1;
+                fx.key[et] = m >= 0 ? (uint32_t)m * A + (uint32_t)id : base_key;
+            }
+            epi_bar();
+            if (et < n) {
+                const uint32_t kt = fx.key[et];
+                int r = 0;
+                for (int u = 0; u < n; ++u) {
+                    const uint32_t ku = fx.key[u];
+                    r += (ku < kt) || (ku == kt && u < et);
+                }
+                fx.perm[r] = et;
+                fx.skey[r] = kt;
+            }
+            epi_bar();
+            const bool head = et < n && (et == 0 || fx.skey[et] != fx.skey[et - 1]);
+            const int incl = warp_incl_scan(head ? 1 : 0);
+            if (lane == 31) ctrl->warp_tot[ew] = incl;
+            epi_bar();
+            int off = 0, tot = 0;
+            for (int w = 0; w < EPI_WARPS; ++w) {
+                if (w < ew) off += ctrl->warp_tot[w];
+                tot += ctrl->warp_tot[w];
+            }
+            if (et < n) {
+                const int s = off + incl - 1;   // segment of sorted row et
+                fx.tok_seg[fx.perm[et]] = s;
+                if (head) {
+                    const uint32_t k = fx.skey[et];
+                    const int rank = (int)(k / A);
+                    fx.seg_start[s] = et;
+                    fx.seg_aid[s] = rank >= RANK_BASE ? -1 : (int)(k - (uint32_t)rank * A);
+                }
+            }
+            if (et == 0) {
+                fx.seg_start[tot] = n;
+                ctrl->n_seg = tot;
+                if (me == 0 && ctrl->bad) atomicOr(a.status, STATUS_BAD_ADAPTER);
+            }
+            epi_bar();
+        }
+        // ---- every call's slots per segment, fetched in one round
+        {
+            const int n_seg = ctrl->n_seg;
+            for (int e = et; e < a.n_calls * NTOK; e += EPI_THREADS) {
+                const int c = e / NTOK, s = e - c * NTOK;
+                if (s >= n_seg) continue;
+                const StepCall &k = a.call[c];
+                const int aid = fx.seg_aid[s];
+                const __nv_bfloat16 *R = nullptr, *Ao = nullptr;
+                int rk = 0;
+                if (aid >= 0) {
+                    const Slot &sl = k.slots[aid];
+                    R = reinterpret_cast<const __nv_bfloat16 *>(sl.R);
+                    if (sl.A && sl.rank > 0 && k.lr_rmax > 0) {
+                        Ao = reinterpret_cast<const __nv_bfloat16 *>(sl.A);
+                        rk = sl.rank;
+                    }
+                }
+                fx.segR[c][s] = R;
+                fx.segA[c][s] = Ao;
+                fx.segRank[c][s] = (uint8_t)rk;
+            }
+            epi_bar();
+            if (ew < a.n_calls) {
+                // warp ew lists call ew's rotated and owned-term segments and
+                // marks its rotated tokens
+                const int c = ew;
+                const uint32_t lt = (1u << lane) - 1u;
+                int no = 0, nl = 0;
+                for (int s0 = 0; s0 < n_seg; s0 += 32) {
+                    const int s = s0 + lane;
+                    const bool o = s < n_seg && fx.segR[c][s] != nullptr;
+                    const bool l = s < n_seg && fx.segA[c][s] != nullptr;
+                    const uint32_t mo = __ballot_sync(0xffffffffu, o), ml = __ballot_sync(0xffffffffu, l);
+                    if (o) fx.oft_list[c][no + __popc(mo & lt)] = (uint8_t)s;
+                    if (l) fx.lr_list[c][nl + __popc(ml & lt)] = (uint8_t)s;
+                    no += __popc(mo);
+                    nl += __popc(ml);
+                }
+                for (int t0 = 0; t0 < NTOK; t0 += 32) {
+                    const int t = t0 + lane;
+                    const bool rot = t < n && fx.segR[c][fx.tok_seg[t]] != nullptr;
+                    const uint32_t m = __ballot_sync(0xffffffffu, rot);
+                    if (lane == 0) fx.oft_mask[c][t0 / 32] = m;
+                }
+                if (lane == 0) {
+                    ctrl->n_oft[c] = no;
+                    ctrl->n_lrs[c] = nl;
+                }
+            }
+            epi_bar();
+        }
+
+        // ---- prologue items
+        float *red = xb;   // shrink reduction scratch
+        for (int it = me; it < a.n_items; it += G) {
+            int c = 0, kind = -1, kk = 0;
+            for (int cc = 0; cc < a.n_calls; ++cc) {
+                const StepCall &k = a.call[cc];
+                if (it >= k.item0 && it < k.item0 + k.copy_items + k.rot_items) {
+                    c = cc;
+                    kk = it - k.item0;
+                    kind = kk < k.copy_items ? 0 : 1;
+                    if (kind == 1) kk -= k.copy_items;
+                    break;
+                }
+                if (it >= k.lr_item0 && it < k.lr_item0 + k.lr_items) {
+                    c = cc;
+                    kk = it - k.lr_item0;
+                    kind = 2;
+                    break;
+                }
+            }
+            if (kind < 0) continue;   // uniform across the CTA
+            const StepCall &k = a.call[c];
+            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
+            __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
+            if (kind == 0) {
+                // copy 8 unrotated token rows x 2048 columns
+                const int ccols = (k.d_in + 2047) / 2048;
+                const int rg = kk / ccols, cc = kk - rg * ccols;
+                const int col = cc * 2048 + et * 8;
+                if (col < k.d_in) {
+                    uint4 buf[8];
+                    bool live[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int t = rg * 8 + r;
+                        live[r] = t < n && !((fx.oft_mask[c][t >> 5] >> (t & 31)) & 1u);
+                        if (live[r]) buf[r] = *reinterpret_cast<const uint4 *>(x + (size_t)t * k.d_in + col);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int t = rg * 8 + r;
+                        if (live[r]) *reinterpret_cast<uint4 *>(xs + (size_t)t * k.kdim + col) = buf[r];
+                    }
+                }
+            } else if (kind == 1) {
+                // rotate the rows of one rotated segment over 16 blocks of 32
+                // features: warp ew takes two; lane l produces column l of a
+                // block from column l of R, the row's 32 inputs arrive by shuffle
+                const int ob = (k.d_in + 511) / 512;
+                const int s_ord = kk / ob, bg = kk - s_ord * ob;
+                if (s_ord < ctrl->n_oft[c]) {
+                    const int seg = fx.oft_list[c][s_ord];
+                    const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
+                    const __nv_bfloat16 *R = fx.segR[c][seg];
+                    const int nblk = k.d_in / OFT_BLK;
+                    float rc[2][OFT_BLK];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int blk = bg * 16 + ew * 2 + i;
+#pragma unroll
+                        for (int m = 0; m < OFT_BLK; ++m)
+                            rc[i][m] = blk < nblk ? __bfloat162float(R[(size_t)blk * OFT_BLK * OFT_BLK + m * OFT_BLK + lane])
+                                                  : 0.f;
+                    }
+                    for (int rb = r0; rb < r1; rb += 4) {
+                        float xv[2][4];
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int blk = bg * 16 + ew * 2 + i;
+#pragma unroll
+                            for (int rr = 0; rr < 4; ++rr)
+                                xv[i][rr] = (blk < nblk && rb + rr < r1)
+                                                ? __bfloat162float(x[(size_t)fx.perm[rb + rr] * k.d_in + blk * OFT_BLK + lane])
+                                                : 0.f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int blk = bg * 16 + ew * 2 + i;
+                            if (blk >= nblk) continue;   // uniform across the warp
+#pragma unroll
+                            for (int rr = 0; rr < 4; ++rr) {
+                                if (rb + rr >= r1) break;
+                                float acc = 0.f;
+#pragma unroll
+                                for (int m = 0; m < OFT_BLK; ++m)
+                                    acc = fmaf(__shfl_sync(0xffffffffu, xv[i][rr], m), rc[i][m], acc);
+                                xs[(size_t)fx.perm[rb + rr] * k.kdim + blk * OFT_BLK + lane] = __float2bfloat16_rn(acc);
+                            }
+                        }
+                    }
+                }
+            } else {
+                // owned low-rank shrink: LR_Q ranks of one segment
+                const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
+                const int s_ord = kk / ng, qg = kk - s_ord * ng;
+                if (s_ord < ctrl->n_lrs[c]) {
+                    const int seg = fx.lr_list[c][s_ord];
+                    const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
+                    const int rk = fx.segRank[c][seg];
+                    const int q0 = qg * LR_Q;
+                    if (q0 < rk) {
+                        const int nq = min(LR_Q, rk - q0);
+                        float *v = k.v;
+                        shrink256(x, k.d_in, fx.perm, r0, r1, fx.segA[c][seg] + (size_t)q0 * k.d_in, nq, red, et,
+                                  [&](int t, int q, float s) { v[(size_t)t * MAX_RANK + q0 + q] = s; });
+                    }
+                }
+            }
+            // publish: the token operand is read by TMA (async proxy)
+            if (kind < 2) fence_proxy_async_global();
+            __threadfence();
+            epi_bar();
+            if (et == 0) atomicAdd(sync + (kind < 2 ? SY_XS : SY_LR) + c, 1);
+        }
+        epi_bar();
+
+        // ---- epilogues, one per segment of this CTA's work, in issue order
+        int buf = 0;
+        uint32_t bph = 0;
+        bool ok = true;
+        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);
+        float *xbm = xb, *xbv = xb + 32 * RED;
+        for (int u = me; ok && u < a.n_units; u += G) {
+            const ULoc U = ulocate(a, u);
+            const StepCall &k = a.call[U.c];
+            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
+            const int nctr = k.vs_chunks;
+            const int u0 = k.vs_unit0 + U.vt * nctr;
+            bool last = true;
+            if (nctr > 1) {
+                publish(tcol, a.part + (size_t)u * SLOT, n, BN, row, half);
+                last = arrive(sync + SY_VTILE + U.c * STEP_MAX_VTILES + U.vt, nctr, ctrl, et);
+            }
+            if (last) {
+                // U[t][q] = (x' A_sh)[t][q] * d_a(t)[q] for VeRA tokens, 0 otherwise
+                stage_meta(a, U.c, fx, ctrl, et);
+                const int r0 = U.vt * TILE_M;
+                __nv_bfloat16 *Ub = reinterpret_cast<__nv_bfloat16 *>(k.U);
+                for (int c32 = 0; c32 * 32 < n; ++c32) {
+                    if (half == 0) {
+                        float v[32];
+                        ptx::tmem_ld32(tcol + c32 * 32, v);
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) xbm[kk * RED + row] = v[kk];
+                    }
+                    epi_bar();
+                    int t[2], q0[2], g[2], kk[2];
+                    bool live[2];
+                    float acc[2][8];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const int it = et + p * EPI_THREADS;
+                        kk[p] = it >> 4;
+                        g[p] = it & 15;
+                        t[p] = c32 * 32 + kk[p];
+                        q0[p] = r0 + g[p] * 8;
+                        live[p] = t[p] < n && q0[p] < k.krv;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[p][e] = xbm[kk[p] * RED + g[p] * 8 + e];
+                    }
+#pragma unroll 4
+                    for (int j = 0; j < nctr; ++j) {
+                        if (u0 + j == u) continue;
+                        const float *src = a.part + (size_t)(u0 + j) * SLOT;
+#pragma unroll
+                        for (int p = 0; p < 2; ++p)
+                            if (live[p]) add_part(src + (size_t)t[p] * TILE_M + g[p] * 8, acc[p]);
+                    }
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        if (!live[p]) continue;
+                        const float *vd = fx.tmeta[t[p]].vd;
+                        uint4 pk;
+                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+                        if (vd && q0[p] < k.rv) {
+                            float d8[8];
+                            ld_vec8(vd + q0[p], true, 0.f, d8);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                p2[e] = __floats2bfloat162_rn(acc[p][2 * e] * d8[2 * e], acc[p][2 * e + 1] * d8[2 * e + 1]);
+                        } else {
+                            pk = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        *reinterpret_cast<uint4 *>(Ub + (size_t)t[p] * k.krv + q0[p]) = pk;
+                    }
+                    epi_bar();
+                }
+                fence_proxy_async_global();
+                __threadfence();
+                epi_bar();
+                if (et == 0) atomicAdd(sync + SY_U + U.c, 1);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
+            if (++buf == 2) { buf = 0; bph ^= 1; }
+        }
+        for (long long b = ms; ok && b < mend;) {
+            const MLoc L = mlocate(a, b);
+            const StepCall &k = a.call[L.c];
+            const long long se = min(mend, L.tb0 + L.nkb);
+            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
+            // contributors: the CTAs between the owners of the tile's first and
+            // last block whose ranges are not empty
+            const int first = owner(fx, G, L.tb0), lastc = owner(fx, G, L.tb0 + L.nkb - 1);
+            int nctr = 0;
+            for (int j = first; j <= lastc; ++j) nctr += fx.start[j + 1] > fx.start[j] ? 1 : 0;
+            const bool my_m = b - L.tb0 < k.kblocks;
+            const bool my_v = k.vkb > 0 && se - L.tb0 > k.kblocks;
+            const int gtile = k.tile0 + L.tile;
+            bool last = true;
+            if (nctr > 1) {
+                float *dst = a.part + (size_t)(a.n_units + gtile + me) * SLOT;
+                if (my_m) publish(tcol, dst, n, BN, row, half);
+                if (my_v) publish(tcol + BN, dst + (size_t)TILE_M * BN, n, BN, row, half);
+                last = arrive(sync + SY_TILE + gtile, nctr, ctrl, et);
+            }
+            if (last) {
+                if (k.lr_rmax > 0 && ctrl->v_call != L.c) {
+                    epi_bar();
+                    if (et == 0) ctrl->flag = wait_count(sync + SY_LR + L.c, k.lr_items, abort_flag, gabort) ? 1 : 0;
+                    epi_bar();
+                    if (!ctrl->flag) ok = false;
+                    if (ok) {
+                        for (int e = et; e < n * k.lr_rmax; e += EPI_THREADS) {
+                            const int t = e / k.lr_rmax, q = e - t * k.lr_rmax;
+                            vsm[t * a.rmax + q] = __ldcg(k.v + (size_t)t * MAX_RANK + q);
+                        }
+                        if (et == 0) ctrl->v_call = L.c;
+                    }
+                    epi_bar();
+                }
+                if (ok) {
+                    stage_meta(a, L.c, fx, ctrl, et);
+                    const int f0 = L.tile * TILE_M;
+                    for (int c32 = 0; c32 * 32 < n; ++c32) {
+                        // half 0 drains the base accumulator, half 1 the VeRA one
+                        if (half == 0 || k.vkb > 0) {
+                            const bool mine = half == 0 ? my_m : my_v;
+                            float *dstp = half == 0 ? xbm : xbv;
+                            if (mine) {
+                                float v[32];
+                                ptx::tmem_ld32(tcol + (half ? BN : 0) + c32 * 32, v);
+#pragma unroll
+                                for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = v[kk];
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = 0.f;
+                            }
+                        }
+                        epi_bar();
+                        int t[2], j0[2], kk[2], g[2];
+                        bool live[2];
+                        float acc[2][8], vacc[2][8];
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+                            const int it = et + p * EPI_THREADS;
+                            kk[p] = it >> 4;
+                            g[p] = it & 15;
+                            t[p] = c32 * 32 + kk[p];
+                            j0[p] = f0 + g[p] * 8;
+                            live[p] = t[p] < n && j0[p] < k.d_out;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                acc[p][e] = xbm[kk[p] * RED + g[p] * 8 + e];
+                                vacc[p][e] = k.vkb > 0 ? xbv[kk[p] * RED + g[p] * 8 + e] : 0.f;
+                            }
+                        }
+                        for (int j = first; j <= lastc; ++j) {
+                            if (j == me || fx.start[j + 1] <= fx.start[j]) continue;
+                            const long long lo = max(L.tb0, fx.start[j]);
+                            const long long hi = min(L.tb0 + L.nkb, fx.start[j + 1]);
+                            const float *src = a.part + (size_t)(a.n_units + gtile + j) * SLOT;
+                            const bool pm = lo - L.tb0 < k.kblocks;
+                            const bool pv = k.vkb > 0 && hi - L.tb0 > k.kblocks;
+#pragma unroll
+                            for (int p = 0; p < 2; ++p) {
+                                if (!live[p]) continue;
+                                const float *sp = src + (size_t)t[p] * TILE_M + g[p] * 8;
+                                if (pm) add_part(sp, acc[p]);
+                                if (pv) add_part(sp + (size_t)TILE_M * BN, vacc[p]);
+                            }
+                        }
+                        const TokMeta *mm[2] = {&fx.tmeta[live[0] ? t[0] : 0], &fx.tmeta[live[1] ? t[1] : 0]};
+                        const float *vr[2] = {vsm + (live[0] ? t[0] : 0) * a.rmax, vsm + (live[1] ? t[1] : 0) * a.rmax};
+                        emit_pair(k, mm, vr, t, j0, live, acc, vacc);
+                        epi_bar();
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
+            if (++buf == 2) { buf = 0; bph ^= 1; }
+            b = se;
+        }
+    }
+
+    // ---- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, NCOLS);
+    }
+    if (threadIdx.x == 0) {
+        if (ctrl->abort) {
+            atomicOr(a.status, STATUS_TIMEOUT);
+            atomicExch(sync + SY_ABORT, 1);
+        }
+        __threadfence();
+        const int old = atomicAdd(sync + SY_EXIT, 1);
+        if (old == G - 1) {
+            // every CTA has left: clear the counters for the next launch
+            __threadfence();
+            const bool aborted = atomicAdd(sync + SY_ABORT, 0) != 0;
+            for (int c = 0; c < a.n_calls; ++c) {
+                sync[SY_XS + c] = 0;
+                sync[SY_LR + c] = 0;
+                sync[SY_U + c] = 0;
+            }
+            if (aborted) {
+                for (int i = 0; i < STEP_MAX_CALLS * STEP_MAX_VTILES; ++i) sync[SY_VTILE + i] = 0;
+                for (int i = 0; i < a.n_tiles; ++i) sync[SY_TILE + i] = 0;
+            }
+            sync[SY_ABORT] = 0;
+            sync[SY_EXIT] = 0;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+size_t step_smem_bytes(int bn, int stages, int rmax) {
+    return 1024 + (size_t)stages * (P_BYTES + bn * 128) + CTRL_BYTES + sizeof(Fixed) + XB_FLOATS * sizeof(float) +
+           (size_t)bn * rmax * sizeof(float);
+}
+
+cudaError_t launch_step(const StepArgs &a, cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = allow_max_dynamic_smem(step_kernel);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.grid, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    // one CTA per SM: a CTA holds up to all 512 TMEM columns and waits on the
+    // others, so two on one SM must never be possible; more than half of the
+    // SM's shared memory guarantees it whatever the register count
+    size_t smem = step_smem_bytes(a.bn, a.stages, a.rmax);
+    if (smem < (size_t)120 * 1024) smem = (size_t)120 * 1024;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeCooperative;
+    attr.val.cooperative = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, step_kernel, a);
+}
+
+}  // namespace scute

@@ -24,8 +24,8 @@ static_assert(SCUTE_NOALLOC_SCRATCH_BYTES == TABLE_OFFSET + SCUTE_NOALLOC_MAX_AD
               "scratch layout: status block, then one int8 per adapter id");
 static_assert(SCUTE_NOALLOC_MAX_ADAPTERS * (N_RANKS) < 65536,
               "the sort packs (method, id) into 16 bits");
-static_assert(SCUTE_LORA == RANK_LORA && SCUTE_DORA == RANK_DORA && SCUTE_IA3 == RANK_IA3 &&
-                  SCUTE_VERA == RANK_VERA && SCUTE_OFT == RANK_OFT && SCUTE_NF == RANK_NF,
+static_assert((int)SCUTE_LORA == (int)RANK_LORA && (int)SCUTE_DORA == (int)RANK_DORA && (int)SCUTE_IA3 == (int)RANK_IA3 &&
+                  (int)SCUTE_VERA == (int)RANK_VERA && (int)SCUTE_OFT == (int)RANK_OFT && (int)SCUTE_NF == (int)RANK_NF,
               "method codes are the kernel's method ranks");
 
 // [0, 4): status word (must start at zero: the kernel only ORs bits into it);

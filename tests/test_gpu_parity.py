@@ -111,6 +111,55 @@ def test_small_decode_parity(scute, out_dtype, n):
     ctx.close()
 
 
+def _batch_run(ctx, w, names, out_dtype, ids=None):
+    """All layers in one scute_linear_batch call (one launch for n <= 128)."""
+    ids_np = w.ids if ids is None else ids
+    ids_t = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).cuda()
+    calls, outs = [], []
+    for name in names:
+        L = w.layer(name)
+        out = torch.full((w.n, L.d_out), float("nan"), device="cuda",
+                         dtype=torch.float32 if out_dtype == "fp32" else torch.bfloat16)
+        calls.append((H.dev(L.get("x")), ctx.layer_ids[name], out))
+        outs.append(out)
+    ctx.linear_batch(calls, ids_t, out_dtype)
+    torch.cuda.synchronize()
+    return outs
+
+
+@pytest.mark.parametrize("n", [2, 50, 128, 200])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_small_decode_batch_parity(scute, out_dtype, n):
+    """Every layer in one batched call; the same layer twice gets its own slot.
+    n <= 128 runs as one persistent launch, n = 200 as consecutive calls."""
+    w = _small_decode(n)
+    ctx = H.make_ctx(scute, w)
+    names = list(SMALL_NAMES) + ["q"]
+    outs = _batch_run(ctx, w, names, out_dtype)
+    assert ctx.sync_status() == 0
+    for name, o in zip(names, outs):
+        H.grade(w, name, o, out_dtype)
+    # the two copies of q are split differently over the CTAs (other K ranges,
+    # other summation order), so they agree to rounding, not bit for bit
+    d = (outs[0].double() - outs[-1].double()).abs().max().item()
+    assert d <= 2e-2
+    ctx.close()
+
+
+def test_decode_full_shapes_batch_sampled(scute):
+    """The Llama-3-8B-shaped decode workload (64 tokens, q, k, v, gate, up,
+    down, 32 mixed adapters) in one batched call, graded on sampled rows."""
+    w = WL.decode_mixed()
+    names = ("q", "k", "v", "gate", "up", "down")
+    ctx = H.make_ctx(scute, w, layer_names=names)
+    outs = _batch_run(ctx, w, names, "fp32")
+    assert ctx.sync_status() == 0
+    rows = [0, 5, 13, 22, 31, 40, 47, 63]
+    for name, o in zip(names, outs):
+        H.grade(w, name, o, "fp32", rows=rows)
+    ctx.close()
+
+
 @pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
 def test_small_prefill_parity(scute, out_dtype):
     """n > 256: tokens on the 128-row side of the tensor-core tile."""
