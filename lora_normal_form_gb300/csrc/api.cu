@@ -354,7 +354,7 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
             return fail(c, SCUTE_ERR_UNSUPPORTED, "rank %d above %d", al.rank, SCUTE_MAX_RANK);
         if (al.s) total += align256(4 * (size_t)L.d_out);
         if (al.b) total += align256(4 * (size_t)L.d_out);
-        if (al.R) total += align256((size_t)L.d_in * OFT_BLK * E);
+        if (al.R) total += align256((size_t)L.d_in * OFT_BLK * E) * (c->dtype == SCUTE_BF16 ? 2 : 1);
         if (al.rank) {
             total += align256((size_t)al.rank * L.d_in * E) + align256((size_t)al.rank * L.d_out * E);
             size_t need = align256((size_t)L.d_in * al.rank * E) + align256((size_t)al.rank * L.d_out * E) +
@@ -448,6 +448,12 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
             void *Rp = take((size_t)L.d_in * OFT_BLK * E);
             REG_TRY(cudaMemcpy(Rp, x.R, (size_t)L.d_in * OFT_BLK * E, cudaMemcpyDefault));
             s.R = Rp;
+            if (c->dtype == SCUTE_BF16) {
+                // the decode step reads R by columns: keep a copy with every block transposed
+                void *Rtp = take((size_t)L.d_in * OFT_BLK * E);
+                REG_TRY(launch_transpose_blocks(Rp, Rtp, L.d_in / OFT_BLK, 0));
+                s.Rt = Rtp;
+            }
         }
         if (al.vera) {
             float *dp = reinterpret_cast<float *>(take(4 * (size_t)L.rv));
@@ -573,7 +579,7 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         if (k.lr_rmax > rmax) rmax = k.lr_rmax;
         k.out_f32 = out_f32;
         k.copy_items = ((nn + 7) / 8) * ((L.d_in + 2047) / 2048);
-        k.rot_items = (L.n_rot < nn ? L.n_rot : nn) * ((L.d_in + 511) / 512);
+        k.rot_items = (L.n_rot < nn ? L.n_rot : nn) * ((L.d_in + 1023) / 1024);
         k.item0 = item;
         item += k.copy_items + k.rot_items;
         k.blk0 = blk;

@@ -33,6 +33,7 @@ struct Slot {
     const void *B;     // owned B' = B diag(e), stored [rank][d_out]
     const float *vd;   // VeRA d [shared rank] (c folded in); null = no shared term
     const float *ve;   // VeRA e [d_out]; null = ones
+    const void *Rt;    // R with every 32x32 block transposed (bf16 contexts; null = no R)
     int rank;          // rank of the owned term (0 = none)
     int pad;
 };
@@ -266,5 +267,7 @@ cudaError_t launch_dora_scale(bool f32, const void *Wt, int kdim, int d_in, int 
                               const void *A, const void *B, int rank, float c,
                               const float *m, float *s_out, int *err, cudaStream_t st);
 cudaError_t launch_scale_vec(const float *v, float c, float *out, int n, cudaStream_t st);
+// dst[b][j][i] = src[b][i][j] for n_blk 32x32 bf16 blocks
+cudaError_t launch_transpose_blocks(const void *src, void *dst, int n_blk, cudaStream_t st);
 
 }  // namespace scute

@@ -125,6 +125,14 @@ __global__ void scale_vec_kernel(const float *v, float c, float *out, int n) {
     if (i < n) out[i] = v[i] * c;
 }
 
+__global__ void transpose_blocks_kernel(const __nv_bfloat16 *src, __nv_bfloat16 *dst) {
+    __shared__ __nv_bfloat16 t[32][33];
+    const size_t b = blockIdx.x;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) t[i][threadIdx.x] = src[b * 1024 + i * 32 + threadIdx.x];
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y) dst[b * 1024 + j * 32 + threadIdx.x] = t[threadIdx.x][j];
+}
+
 int blocks_for(size_t total, int threads) {
     size_t b = (total + threads - 1) / threads;
     return (int)(b > 4096 ? 4096 : (b < 1 ? 1 : b));
@@ -189,6 +197,14 @@ cudaError_t launch_dora_scale(bool f32, const void *Wt, int kdim, int d_in, int 
 cudaError_t launch_scale_vec(const float *v, float c, float *out, int n, cudaStream_t st) {
     (void)cudaGetLastError();
     scale_vec_kernel<<<(n + 255) / 256, 256, 0, st>>>(v, c, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_blocks(const void *src, void *dst, int n_blk, cudaStream_t st) {
+    (void)cudaGetLastError();
+    if (n_blk <= 0) return cudaSuccess;
+    transpose_blocks_kernel<<<n_blk, dim3(32, 8), 0, st>>>(reinterpret_cast<const __nv_bfloat16 *>(src),
+                                                         reinterpret_cast<__nv_bfloat16 *>(dst));
     return cudaGetLastError();
 }
 

@@ -51,8 +51,6 @@ constexpr int MAX_STAGES = 8;
 constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s per wait
 constexpr int RED = TILE_M + 4;               // token-row stride of a transposed chunk (floats)
 constexpr int XB_FLOATS = 2 * 32 * RED;       // main + VeRA chunk of 32 tokens
-constexpr int PF_AHEAD = 24;                  // K blocks of W asked from L2 at start
-constexpr int PF_CHUNK = 24;                  // K blocks per L2 request run
 constexpr int NTOK = STEP_MAX_TOKENS;
 constexpr int NCALL = STEP_MAX_CALLS;
 constexpr int LR_Q = 8;                       // ranks per low-rank shrink item
@@ -88,6 +86,7 @@ struct Ctrl {
     int bad;
     int warp_tot[EPI_WARPS];
     int n_oft[NCALL], n_lrs[NCALL];
+    int done[2][NCALL];   // prologue items this CTA finished per call: token operand, low-rank
 };
 constexpr int CTRL_BYTES = 512;
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
@@ -107,7 +106,7 @@ struct Fixed {
     int tok_aid[NTOK];                    // token -> adapter (-1: base only)
     int tok_seg[NTOK];                    // token -> segment
     int seg_start[NTOK + 1], seg_aid[NTOK];
-    const __nv_bfloat16 *segR[NCALL][NTOK];   // per call: rotation of each segment (null: none)
+    const __nv_bfloat16 *segR[NCALL][NTOK];   // per call: transposed rotation of each segment (null: none)
     const __nv_bfloat16 *segA[NCALL][NTOK];   // per call: owned A' of each segment (null: none)
     uint8_t segRank[NCALL][NTOK];
     uint8_t oft_list[NCALL][NTOK];            // per call: segments with a rotation
@@ -320,63 +319,6 @@ __device__ __forceinline__ void add_part(const float *src, float (&acc)[8]) {
     acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
 }
 
-// Two output items (token t[p], features [j0[p], j0[p]+8)) of one layer:
-// y = acc * s + b + v B'[:, j0:j0+8] + vacc * e, every independent load of
-// both items issued before any of them is used.
-__device__ __forceinline__ void emit_pair(const StepCall &k, const TokMeta *const (&m)[2],
-                                          const float *const (&vrow)[2], const int (&t)[2], const int (&j0)[2],
-                                          const bool (&live)[2], float (&acc)[2][8], const float (&vacc)[2][8]) {
-    float y[2][8];
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        float s8[8], b8[8], e8[8];
-        ld_vec8(m[p]->s + j0[p], live[p] && m[p]->s, 1.f, s8);
-        ld_vec8(m[p]->b + j0[p], live[p] && m[p]->b, 0.f, b8);
-        ld_vec8(m[p]->ve + j0[p], live[p] && m[p]->ve, 1.f, e8);
-        const float vs = m[p]->vera ? 1.f : 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[p][q] = fmaf(acc[p][q], s8[q], b8[q]) + vs * vacc[p][q] * e8[q];
-    }
-    const int r0 = live[0] ? m[0]->rank : 0, r1 = live[1] ? m[1]->rank : 0;
-    const int rmax = r0 > r1 ? r0 : r1;
-    for (int q0 = 0; q0 < rmax; q0 += 8) {
-        uint4 bq[2][8];
-#pragma unroll
-        for (int p = 0; p < 2; ++p)
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (q0 + q < (p ? r1 : r0))
-                    bq[p][q] = __ldg(reinterpret_cast<const uint4 *>(m[p]->B + j0[p] + (size_t)(q0 + q) * k.d_out));
-#pragma unroll
-        for (int p = 0; p < 2; ++p)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (q0 + q < (p ? r1 : r0)) {
-                    const float vq = vrow[p][q0 + q];
-                    float bf[8];
-                    unpack8(bq[p][q], bf);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) y[p][e] = fmaf(vq, bf[e], y[p][e]);
-                }
-            }
-    }
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        if (!live[p]) continue;
-        if (k.out_f32) {
-            float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(k.out) + (size_t)t[p] * k.d_out + j0[p]);
-            o[0] = make_float4(y[p][0], y[p][1], y[p][2], y[p][3]);
-            o[1] = make_float4(y[p][4], y[p][5], y[p][6], y[p][7]);
-        } else {
-            uint4 pk;
-            __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[p][2 * e], y[p][2 * e + 1]);
-            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(k.out) + (size_t)t[p] * k.d_out + j0[p]) = pk;
-        }
-    }
-}
-
 // x_i A_rows^T for up to LR_Q rows of A (each [d_in], bf16) and the sorted
 // rows [r0, r1) (tokens perm[r]); emit(token, q, value) once per (row, q).
 // Each of the 256 threads covers 8 consecutive k per pass; a warp reduces its
@@ -394,22 +336,35 @@ __device__ void shrink256(const __nv_bfloat16 *x, int d_in, const int *perm, int
         const __nv_bfloat16 *xr[LR_ROWS];
 #pragma unroll
         for (int r = 0; r < LR_ROWS; ++r) xr[r] = x + (size_t)perm[rc + (r < nr ? r : 0)] * d_in;
-#pragma unroll 2
-        for (int kk = et * 8; kk < d_in; kk += EPI_THREADS * 8) {
-            uint4 au[LR_Q], xu[LR_ROWS];
+        // one pass of 8 k per thread per iteration; the next iteration's
+        // operands are loaded while the current ones are multiplied, and the
+        // loop stays rolled so that its code is short
+        uint4 au[LR_Q], xu[LR_ROWS];
+        auto load = [&](int k0) {
+            const bool in = k0 < d_in;
 #pragma unroll
             for (int q = 0; q < LR_Q; ++q)
-                au[q] = q < nq ? *reinterpret_cast<const uint4 *>(Arows + (size_t)q * d_in + kk) : make_uint4(0u, 0u, 0u, 0u);
+                au[q] = (in && q < nq) ? *reinterpret_cast<const uint4 *>(Arows + (size_t)q * d_in + k0) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int r = 0; r < LR_ROWS; ++r)
-                xu[r] = r < nr ? *reinterpret_cast<const uint4 *>(xr[r] + kk) : make_uint4(0u, 0u, 0u, 0u);
+                xu[r] = (in && r < nr) ? *reinterpret_cast<const uint4 *>(xr[r] + k0) : make_uint4(0u, 0u, 0u, 0u);
+        };
+        load(et * 8);
+#pragma unroll 1
+        for (int kk = et * 8; kk < d_in; kk += EPI_THREADS * 8) {
+            uint4 ca[LR_Q], cx[LR_ROWS];
+#pragma unroll
+            for (int q = 0; q < LR_Q; ++q) ca[q] = au[q];
+#pragma unroll
+            for (int r = 0; r < LR_ROWS; ++r) cx[r] = xu[r];
+            load(kk + EPI_THREADS * 8);
             float xv[LR_ROWS][8];
 #pragma unroll
-            for (int r = 0; r < LR_ROWS; ++r) unpack8(xu[r], xv[r]);
+            for (int r = 0; r < LR_ROWS; ++r) unpack8(cx[r], xv[r]);
 #pragma unroll
             for (int q = 0; q < LR_Q; ++q) {
                 float av[8];
-                unpack8(au[q], av);
+                unpack8(ca[q], av);
 #pragma unroll
                 for (int r = 0; r < LR_ROWS; ++r)
 #pragma unroll
@@ -473,6 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         ctrl->abort = 0;
         ctrl->meta_call = ctrl->v_call = -1;
         ctrl->bad = 0;
+        for (int c = 0; c < NCALL; ++c) ctrl->done[0][c] = ctrl->done[1][c] = 0;
         ptx::fence_mbar_init();
     }
     for (int i = threadIdx.x; i <= G; i += THREADS) fx.start[i] = a.start[i];
@@ -713,24 +669,33 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         // ---- every call's slots per segment, fetched in one round
         {
             const int n_seg = ctrl->n_seg;
-            for (int e = et; e < a.n_calls * NTOK; e += EPI_THREADS) {
-                const int c = e / NTOK, s = e - c * NTOK;
-                if (s >= n_seg) continue;
-                const StepCall &k = a.call[c];
-                const int aid = fx.seg_aid[s];
-                const __nv_bfloat16 *R = nullptr, *Ao = nullptr;
-                int rk = 0;
+            constexpr int PER = NCALL * NTOK / EPI_THREADS;
+            const __nv_bfloat16 *R[PER], *Ao[PER];
+            int rk[PER];
+            // every slot load of this thread is issued before any is used
+#pragma unroll
+            for (int r = 0; r < PER; ++r) {
+                const int e = et + r * EPI_THREADS, c = e / NTOK, s = e - c * NTOK;
+                const int aid = (c < a.n_calls && s < n_seg) ? fx.seg_aid[s] : -1;
+                R[r] = Ao[r] = nullptr;
+                rk[r] = 0;
                 if (aid >= 0) {
+                    const StepCall &k = a.call[c];
                     const Slot &sl = k.slots[aid];
-                    R = reinterpret_cast<const __nv_bfloat16 *>(sl.R);
+                    R[r] = reinterpret_cast<const __nv_bfloat16 *>(sl.Rt);
                     if (sl.A && sl.rank > 0 && k.lr_rmax > 0) {
-                        Ao = reinterpret_cast<const __nv_bfloat16 *>(sl.A);
-                        rk = sl.rank;
+                        Ao[r] = reinterpret_cast<const __nv_bfloat16 *>(sl.A);
+                        rk[r] = sl.rank;
                     }
                 }
-                fx.segR[c][s] = R;
-                fx.segA[c][s] = Ao;
-                fx.segRank[c][s] = (uint8_t)rk;
+            }
+#pragma unroll
+            for (int r = 0; r < PER; ++r) {
+                const int e = et + r * EPI_THREADS, c = e / NTOK, s = e - c * NTOK;
+                if (c >= a.n_calls || s >= n_seg) continue;
+                fx.segR[c][s] = R[r];
+                fx.segA[c][s] = Ao[r];
+                fx.segRank[c][s] = (uint8_t)rk[r];
             }
             epi_bar();
             if (ew < a.n_calls) {
@@ -765,6 +730,18 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
 
         // ---- prologue items
         float *red = xb;   // shrink reduction scratch
+        // completed items are published once per kind and CTA: every thread's
+        // writes made visible (the token operand is read by TMA, the async
+        // proxy), then one counter add per call
+        auto release_items = [&](int which) {
+            if (which == 0) fence_proxy_async_global();
+            __threadfence();
+            epi_bar();
+            if (et == 0)
+                for (int c = 0; c < a.n_calls; ++c)
+                    if (ctrl->done[which][c]) atomicAdd(sync + (which ? SY_LR : SY_XS) + c, ctrl->done[which][c]);
+        };
+        bool xs_published = false;
         for (int it = me; it < a.n_items; it += G) {
             int c = 0, kind = -1, kk = 0;
             for (int cc = 0; cc < a.n_calls; ++cc) {
@@ -784,6 +761,10 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 }
             }
             if (kind < 0) continue;   // uniform across the CTA
+            if (kind == 2 && !xs_published) {
+                release_items(0);
+                xs_published = true;
+            }
             const StepCall &k = a.call[c];
             const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
             __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
@@ -808,47 +789,56 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     }
                 }
             } else if (kind == 1) {
-                // rotate the rows of one rotated segment over 16 blocks of 32
-                // features: warp ew takes two; lane l produces column l of a
-                // block from column l of R, the row's 32 inputs arrive by shuffle
-                const int ob = (k.d_in + 511) / 512;
+                // rotate the rows of one rotated segment over 32 blocks of 32
+                // features: warp ew takes four, one after the other; lane l
+                // produces column l of a block from row l of the transposed
+                // block (four 16-byte loads) and the row's 32 inputs, which
+                // arrive by shuffle.  The next block's operands are loaded
+                // while the current one is computed; the loops stay rolled, so
+                // the code is short.
+                const int ob = (k.d_in + 1023) / 1024;
                 const int s_ord = kk / ob, bg = kk - s_ord * ob;
                 if (s_ord < ctrl->n_oft[c]) {
                     const int seg = fx.oft_list[c][s_ord];
                     const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
-                    const __nv_bfloat16 *R = fx.segR[c][seg];
+                    const __nv_bfloat16 *Rt = fx.segR[c][seg];
                     const int nblk = k.d_in / OFT_BLK;
-                    float rc[2][OFT_BLK];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int blk = bg * 16 + ew * 2 + i;
-#pragma unroll
-                        for (int m = 0; m < OFT_BLK; ++m)
-                            rc[i][m] = blk < nblk ? __bfloat162float(R[(size_t)blk * OFT_BLK * OFT_BLK + m * OFT_BLK + lane])
-                                                  : 0.f;
-                    }
+                    const int b0 = bg * 32 + ew * 4;
+                    const int nb = max(0, min(4, nblk - b0));
                     for (int rb = r0; rb < r1; rb += 4) {
-                        float xv[2][4];
+                        const int nr = min(4, r1 - rb);
+                        uint4 rq[4];
+                        float xv[4];
+                        auto load = [&](int blk) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(Rt + (size_t)blk * OFT_BLK * OFT_BLK + lane * OFT_BLK);
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const int blk = bg * 16 + ew * 2 + i;
+                            for (int u = 0; u < 4; ++u) rq[u] = src[u];
 #pragma unroll
                             for (int rr = 0; rr < 4; ++rr)
-                                xv[i][rr] = (blk < nblk && rb + rr < r1)
-                                                ? __bfloat162float(x[(size_t)fx.perm[rb + rr] * k.d_in + blk * OFT_BLK + lane])
-                                                : 0.f;
-                        }
+                                xv[rr] = rr < nr ? __bfloat162float(x[(size_t)fx.perm[rb + rr] * k.d_in + blk * OFT_BLK + lane]) : 0.f;
+                        };
+                        if (nb > 0) load(b0);
+#pragma unroll 1
+                        for (int i = 0; i < nb; ++i) {
+                            float rc[OFT_BLK];
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            const int blk = bg * 16 + ew * 2 + i;
-                            if (blk >= nblk) continue;   // uniform across the warp
+                            for (int u = 0; u < 4; ++u) {
+                                float f8[8];
+                                unpack8(rq[u], f8);
 #pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) {
-                                if (rb + rr >= r1) break;
+                                for (int e = 0; e < 8; ++e) rc[u * 8 + e] = f8[e];
+                            }
+                            float xc[4];
+#pragma unroll
+                            for (int rr = 0; rr < 4; ++rr) xc[rr] = xv[rr];
+                            if (i + 1 < nb) load(b0 + i + 1);
+                            const int blk = b0 + i;
+#pragma unroll 1
+                            for (int rr = 0; rr < nr; ++rr) {
+                                const float xr = rr == 0 ? xc[0] : rr == 1 ? xc[1] : rr == 2 ? xc[2] : xc[3];
                                 float acc = 0.f;
 #pragma unroll
-                                for (int m = 0; m < OFT_BLK; ++m)
-                                    acc = fmaf(__shfl_sync(0xffffffffu, xv[i][rr], m), rc[i][m], acc);
+                                for (int m = 0; m < OFT_BLK; ++m) acc = fmaf(__shfl_sync(0xffffffffu, xr, m), rc[m], acc);
                                 xs[(size_t)fx.perm[rb + rr] * k.kdim + blk * OFT_BLK + lane] = __float2bfloat16_rn(acc);
                             }
                         }
@@ -871,12 +861,10 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     }
                 }
             }
-            // publish: the token operand is read by TMA (async proxy)
-            if (kind < 2) fence_proxy_async_global();
-            __threadfence();
-            epi_bar();
-            if (et == 0) atomicAdd(sync + (kind < 2 ? SY_XS : SY_LR) + c, 1);
+            if (et == 0) ++ctrl->done[kind == 2 ? 1 : 0][c];
         }
+        if (!xs_published) release_items(0);
+        release_items(1);
         epi_bar();
 
         // ---- epilogues, one per segment of this CTA's work, in issue order
@@ -904,7 +892,10 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 const int r0 = U.vt * TILE_M;
                 __nv_bfloat16 *Ub = reinterpret_cast<__nv_bfloat16 *>(k.U);
                 for (int c32 = 0; c32 * 32 < n; ++c32) {
-                    if (half == 0) {
+                    // a lone contributor's tile comes from TMEM; otherwise every
+                    // published partial is summed in unit order, this CTA's too,
+                    // so the result does not depend on which CTA finished last
+                    if (half == 0 && nctr == 1) {
                         float v[32];
                         ptx::tmem_ld32(tcol + c32 * 32, v);
 #pragma unroll
@@ -923,11 +914,10 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                         q0[p] = r0 + g[p] * 8;
                         live[p] = t[p] < n && q0[p] < k.krv;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[p][e] = xbm[kk[p] * RED + g[p] * 8 + e];
+                        for (int e = 0; e < 8; ++e) acc[p][e] = nctr == 1 ? xbm[kk[p] * RED + g[p] * 8 + e] : 0.f;
                     }
 #pragma unroll 4
-                    for (int j = 0; j < nctr; ++j) {
-                        if (u0 + j == u) continue;
+                    for (int j = 0; j < (nctr > 1 ? nctr : 0); ++j) {
                         const float *src = a.part + (size_t)(u0 + j) * SLOT;
 #pragma unroll
                         for (int p = 0; p < 2; ++p)
@@ -1003,56 +993,119 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     stage_meta(a, L.c, fx, ctrl, et);
                     const int f0 = L.tile * TILE_M;
                     for (int c32 = 0; c32 * 32 < n; ++c32) {
-                        // half 0 drains the base accumulator, half 1 the VeRA one
-                        if (half == 0 || k.vkb > 0) {
-                            const bool mine = half == 0 ? my_m : my_v;
+                        // a lone contributor's tile comes from TMEM (half 0 drains
+                        // the base accumulator, half 1 the VeRA one); otherwise
+                        // every published partial is summed in CTA order, this
+                        // CTA's too, so the result does not depend on which CTA
+                        // finished last
+                        if (nctr == 1 && (half == 0 || k.vkb > 0)) {
                             float *dstp = half == 0 ? xbm : xbv;
-                            if (mine) {
-                                float v[32];
-                                ptx::tmem_ld32(tcol + (half ? BN : 0) + c32 * 32, v);
+                            float v[32];
+                            ptx::tmem_ld32(tcol + (half ? BN : 0) + c32 * 32, v);
 #pragma unroll
-                                for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = v[kk];
-                            } else {
-#pragma unroll
-                                for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = 0.f;
-                            }
+                            for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = v[kk];
                         }
                         epi_bar();
-                        int t[2], j0[2], kk[2], g[2];
-                        bool live[2];
-                        float acc[2][8], vacc[2][8];
-#pragma unroll
+#pragma unroll 1
                         for (int p = 0; p < 2; ++p) {
                             const int it = et + p * EPI_THREADS;
-                            kk[p] = it >> 4;
-                            g[p] = it & 15;
-                            t[p] = c32 * 32 + kk[p];
-                            j0[p] = f0 + g[p] * 8;
-                            live[p] = t[p] < n && j0[p] < k.d_out;
+                            const int kk = it >> 4, g = it & 15;
+                            const int t = c32 * 32 + kk, j0 = f0 + g * 8;
+                            if (t >= n || j0 >= k.d_out) continue;
+                            const TokMeta &m = fx.tmeta[t];
+                            // the slot operands do not depend on the sums: ask for them first
+                            float s8[8], b8[8], e8[8];
+                            ld_vec8(m.s + j0, m.s != nullptr, 1.f, s8);
+                            ld_vec8(m.b + j0, m.b != nullptr, 0.f, b8);
+                            ld_vec8(m.ve + j0, m.ve != nullptr, 1.f, e8);
+                            uint4 bq[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)q * k.d_out));
+                            float acc[8], vacc[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                acc[p][e] = xbm[kk[p] * RED + g[p] * 8 + e];
-                                vacc[p][e] = k.vkb > 0 ? xbv[kk[p] * RED + g[p] * 8 + e] : 0.f;
+                                acc[e] = nctr == 1 ? xbm[kk * RED + g * 8 + e] : 0.f;
+                                vacc[e] = (nctr == 1 && k.vkb > 0) ? xbv[kk * RED + g * 8 + e] : 0.f;
                             }
-                        }
-                        for (int j = first; j <= lastc; ++j) {
-                            if (j == me || fx.start[j + 1] <= fx.start[j]) continue;
-                            const long long lo = max(L.tb0, fx.start[j]);
-                            const long long hi = min(L.tb0 + L.nkb, fx.start[j + 1]);
-                            const float *src = a.part + (size_t)(a.n_units + gtile + j) * SLOT;
-                            const bool pm = lo - L.tb0 < k.kblocks;
-                            const bool pv = k.vkb > 0 && hi - L.tb0 > k.kblocks;
+                            // the contributors' partial tiles, two at a time, in CTA order
+                            for (int jb = first; nctr > 1 && jb <= lastc; jb += 2) {
+                                float4 pm[2][2], pv[2][2];
+                                bool om[2], ov[2];
 #pragma unroll
-                            for (int p = 0; p < 2; ++p) {
-                                if (!live[p]) continue;
-                                const float *sp = src + (size_t)t[p] * TILE_M + g[p] * 8;
-                                if (pm) add_part(sp, acc[p]);
-                                if (pv) add_part(sp + (size_t)TILE_M * BN, vacc[p]);
+                                for (int u = 0; u < 2; ++u) {
+                                    const int j = jb + u;
+                                    const bool valid = j <= lastc && fx.start[j + 1] > fx.start[j];
+                                    const long long lo = valid ? max(L.tb0, fx.start[j]) : 0;
+                                    const long long hi = valid ? min(L.tb0 + L.nkb, fx.start[j + 1]) : 0;
+                                    om[u] = valid && lo - L.tb0 < k.kblocks;
+                                    ov[u] = valid && k.vkb > 0 && hi - L.tb0 > k.kblocks;
+                                    const float *sp = a.part + (size_t)(a.n_units + gtile + j) * SLOT + (size_t)t * TILE_M + g * 8;
+                                    if (om[u]) {
+                                        pm[u][0] = __ldcg(reinterpret_cast<const float4 *>(sp));
+                                        pm[u][1] = __ldcg(reinterpret_cast<const float4 *>(sp + 4));
+                                    }
+                                    if (ov[u]) {
+                                        pv[u][0] = __ldcg(reinterpret_cast<const float4 *>(sp + (size_t)TILE_M * BN));
+                                        pv[u][1] = __ldcg(reinterpret_cast<const float4 *>(sp + (size_t)TILE_M * BN + 4));
+                                    }
+                                }
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    if (om[u]) {
+                                        acc[0] += pm[u][0].x; acc[1] += pm[u][0].y; acc[2] += pm[u][0].z; acc[3] += pm[u][0].w;
+                                        acc[4] += pm[u][1].x; acc[5] += pm[u][1].y; acc[6] += pm[u][1].z; acc[7] += pm[u][1].w;
+                                    }
+                                    if (ov[u]) {
+                                        vacc[0] += pv[u][0].x; vacc[1] += pv[u][0].y; vacc[2] += pv[u][0].z; vacc[3] += pv[u][0].w;
+                                        vacc[4] += pv[u][1].x; vacc[5] += pv[u][1].y; vacc[6] += pv[u][1].z; vacc[7] += pv[u][1].w;
+                                    }
+                                }
+                            }
+                            // y = acc * s + b + v B'[:, j0:j0+8] + vacc * e
+                            const float *vrow = vsm + t * a.rmax;
+                            const float vs = m.vera ? 1.f : 0.f;
+                            float y[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) y[e] = fmaf(acc[e], s8[e], b8[e]) + vs * vacc[e] * e8[e];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                if (q < m.rank) {
+                                    float bf[8];
+                                    unpack8(bq[q], bf);
+                                    const float vq = vrow[q];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
+                                }
+                            }
+#pragma unroll 1
+                            for (int q0 = 8; q0 < m.rank; q0 += 8) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)(q0 + q) * k.d_out));
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    if (q0 + q < m.rank) {
+                                        float bf[8];
+                                        unpack8(bq[q], bf);
+                                        const float vq = vrow[q0 + q];
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
+                                    }
+                                }
+                            }
+                            if (k.out_f32) {
+                                float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(k.out) + (size_t)t * k.d_out + j0);
+                                o[0] = make_float4(y[0], y[1], y[2], y[3]);
+                                o[1] = make_float4(y[4], y[5], y[6], y[7]);
+                            } else {
+                                uint4 pk;
+                                __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(k.out) + (size_t)t * k.d_out + j0) = pk;
                             }
                         }
-                        const TokMeta *mm[2] = {&fx.tmeta[live[0] ? t[0] : 0], &fx.tmeta[live[1] ? t[1] : 0]};
-                        const float *vr[2] = {vsm + (live[0] ? t[0] : 0) * a.rmax, vsm + (live[1] ? t[1] : 0) * a.rmax};
-                        emit_pair(k, mm, vr, t, j0, live, acc, vacc);
                         epi_bar();
                     }
                 }

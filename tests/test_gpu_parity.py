@@ -146,6 +146,19 @@ def test_small_decode_batch_parity(scute, out_dtype, n):
     ctx.close()
 
 
+def test_batch_repeats_bit_for_bit(scute):
+    """Partial tiles are summed in a fixed order, whichever CTA finishes a tile,
+    so repeated calls give identical bits."""
+    w = _small_decode(64)
+    ctx = H.make_ctx(scute, w)
+    first = _batch_run(ctx, w, SMALL_NAMES, "bf16")
+    for _ in range(4):
+        again = _batch_run(ctx, w, SMALL_NAMES, "bf16")
+        for name, a, b in zip(SMALL_NAMES, first, again):
+            assert torch.equal(a, b), name
+    ctx.close()
+
+
 def test_decode_full_shapes_batch_sampled(scute):
     """The Llama-3-8B-shaped decode workload (64 tokens, q, k, v, gate, up,
     down, 32 mixed adapters) in one batched call, graded on sampled rows."""
