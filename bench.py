@@ -49,6 +49,22 @@ WORKLOAD = ("decode_mixed: Llama-3-8B-shaped q,k,v,gate,up,down; n=64 tokens; 32
             "OFT block 32; ids uniform")
 
 
+def captured_traffic():
+    """DRAM bytes (read + write) per launch of the step kernel from the committed
+    ncu summary, or None when the kernel source has changed since that capture."""
+    import hashlib
+    import re
+    try:
+        md = open(os.path.join(ROOT, "profiles", "step_kernel_decode_mixed_ncu_full.md")).read()
+        src = open(os.path.join(ROOT, "lora_normal_form_gb300", "csrc", "k_step.cu"), "rb").read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes=(\d+) k_step_sha16=([0-9a-f]{16})", md)
+    if not m or hashlib.sha256(src).hexdigest()[:16] != m.group(2):
+        return None
+    return int(m.group(1))
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -56,6 +72,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="scute", choices=["scute", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--eager-steps", type=int, default=0,
+                   help="only run this many untimed batched steps of the mixed workload and exit "
+                        "(a fixed launch sequence for profilers); prints no JSON line")
     return p.parse_args()
 
 
@@ -214,6 +233,17 @@ def main():
 
     ctx = scute.Context("bf16", max_tokens=64, max_adapters=40, max_layers=8, device=local_rank)
     ctx.load_workload(w)
+    if args.eager_steps > 0:
+        xs = {p: to_dev(w.layer(p).get("x")) for p in PROJ}
+        ids = torch.from_numpy(w.ids.copy()).to(dev)
+        outs = {p: torch.empty(w.n, w.layer(p).d_out, dtype=torch.bfloat16, device=dev) for p in PROJ}
+        for _ in range(args.eager_steps):
+            ctx.linear_batch([(xs[p], ctx.layer_ids[p], outs[p]) for p in PROJ], ids, "bf16")
+        torch.cuda.synchronize()
+        if ctx.sync_status() != 0:
+            raise RuntimeError("device status error")
+        ctx.close()
+        return
     ctx_l = scute.Context("bf16", max_tokens=64, max_adapters=40, max_layers=8, device=local_rank)
     ctx_l.load_workload(wl)
     xs = {p: to_dev(w.layer(p).get("x")) for p in PROJ}
@@ -366,7 +396,7 @@ def main():
         "overhead_vs_all_lora_pct": 100.0 * (ms / ms_lora - 1.0),
         "roofline": {"kernel": "decode step (tcgen05 + TMA, one persistent launch per step)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_kind": peak_kind, "traffic": None, "kernel_ms": kernel_ms,
+                     "peak_kind": peak_kind, "traffic": captured_traffic(), "kernel_ms": kernel_ms,
                      "algorithmic_bytes_per_launch": alg_bytes},
         "block_groups_ms_per_step": float(np.mean(t_grouped)),
         "separate_calls_ms_per_step": float(np.mean(t_calls)),
