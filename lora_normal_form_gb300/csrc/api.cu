@@ -700,44 +700,9 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
 
     const int lr_rmax = L.n_lr > 0 ? max_owned_rank(c, layer) : 0;
     const bool vera_on = L.rv > 0 && L.n_vera > 0;
-    // Decode batches (bf16, n <= 128): one prologue launch (indexing, rotation,
-    // both shrinks) and one GEMM whose epilogue applies s, b, the owned
-    // low-rank expand and the VeRA expand (as extra tcgen05 K blocks).
-    const bool fused = !f32 && nn <= 128;
-    if (fused) {
-        PrepArgs pa;
-        memset(&pa, 0, sizeof(pa));
-        pa.x = x;
-        pa.d_in = L.d_in;
-        pa.n = nn;
-        pa.kdim = L.kdim;
-        pa.ids = ids;
-        pa.method_tab = c->d_method;
-        pa.A = c->max_adapters;
-        pa.slots = slots;
-        pa.perm = c->d_perm;
-        pa.aid_s = c->d_aid;
-        pa.seg_start = c->d_seg_start;
-        pa.seg_aid = c->d_seg_aid;
-        pa.meta = c->d_meta;
-        pa.status = c->d_status;
-        pa.xs = c->xs;
-        pa.v = c->v_part;
-        pa.v_ld = MAX_RANK;
-        pa.U = c->U;
-        pa.u_ld = L.krv;
-        pa.Ash = L.Ash;
-        pa.rv = vera_on ? L.rv : 0;
-        // rotation items: per 256-column chunk, one copy item plus one item per
-        // rotated segment the batch can hold
-        const int rot_segs = L.n_rot < nn ? L.n_rot : nn;
-        pa.n_rot = ((L.d_in + 255) / 256) * (1 + rot_segs);
-        pa.lr_groups = lr_rmax > 0 ? (lr_rmax + 3) / 4 : 1;
-        pa.n_lr = lr_rmax > 0 ? (nn < L.n_lr ? nn : L.n_lr) * pa.lr_groups : 0;
-        pa.n_vera = vera_on ? (L.rv + 3) / 4 : 0;
-        CU_TRY(c, launch_prep(pa, pa.n_rot + pa.n_lr + pa.n_vera, st, c->pdl));
-        ++k;
-    } else {
+    // Other batches (fp32 contexts, or more than STEP_MAX_TOKENS tokens): one
+    // launch per step.
+    {
         // 1. token indexing
         CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
                                c->d_seg_aid, c->d_meta, c->d_status, st));
@@ -747,7 +712,7 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
                                        c->pdl));
         ++k;
     }
-    // 3. base GEMM with the s / b epilogue (and the fused terms)
+    // 3. base GEMM with the s / b epilogue
     const bool tok_on_p = nn > 256;
     GemmArgs g;
     memset(&g, 0, sizeof(g));
@@ -769,18 +734,6 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         g.p_base = L.Wt;
         g.p_pitch = (long long)L.kdim * c->esz;
         g.p_rows = L.d_out;
-    }
-    if (fused) {
-        if (lr_rmax > 0) {
-            g.v = c->v_part;
-            g.v_ld = MAX_RANK;
-            g.lr_rmax = lr_rmax;
-        }
-        if (vera_on) {
-            g.mapVP = L.mapBsh;
-            g.mapVQ = L.mapU;
-            g.vera_kb = (L.krv * c->esz + 127) / 128;
-        }
     }
     GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms, g.lr_rmax);
     g.splits = p.splits;
@@ -810,7 +763,7 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     }
     ++k;
     // 4. owned low-rank shrink / expand
-    if (L.n_lr > 0 && !fused) {
+    if (L.n_lr > 0) {
         int bound = nn;
         int reg = 0;
         for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
@@ -821,7 +774,7 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         k += 2;
     }
     // 5. VeRA: shared shrink then shared expand over the VeRA rows only
-    if (vera_on && !fused) {
+    if (vera_on) {
         GemmArgs v;
         memset(&v, 0, sizeof(v));
         v.mapP = tok_on_p ? L.mapXs : L.mapAsh;

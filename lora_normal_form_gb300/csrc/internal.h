@@ -141,30 +141,6 @@ cudaError_t allow_max_dynamic_smem(K kernel) {
     return e;
 }
 
-// ---------------------------------------------------------------- decode prologue
-constexpr int PREP_MAX_TOKENS = 256;
-
-struct PrepArgs {
-    const void *x;             // [n, d_in] bf16, token order
-    int d_in, n, kdim;
-    const int32_t *ids;
-    const int8_t *method_tab;
-    int A;                     // max adapters
-    const Slot *slots;         // this layer's slot row
-    int *perm, *aid_s, *seg_start, *seg_aid;
-    IndexMeta *meta;
-    int *status;
-    void *xs;                  // [max_tokens, kdim] sorted, rotated token operand
-    float *v;                  // [max_tokens, v_ld] owned low-rank intermediate
-    int v_ld;
-    void *U;                   // [max_tokens, u_ld] bf16 VeRA intermediate (d applied)
-    int u_ld;
-    const void *Ash;           // [rv, d_in] shared VeRA A, K-major
-    int rv;
-    int n_rot, n_lr, lr_groups, n_vera;   // work items per kind (grid = their sum)
-};
-size_t prep_smem_bytes();
-cudaError_t launch_prep(const PrepArgs &p, int grid, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- decode step
 // Every projection of one batched call (up to STEP_MAX_CALLS layers over the
