@@ -578,10 +578,6 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         k.lr_rmax = L.n_lr > 0 ? max_owned_rank(c, calls[i].layer) : 0;
         if (k.lr_rmax > rmax) rmax = k.lr_rmax;
         k.out_f32 = out_f32;
-        k.copy_items = ((nn + 7) / 8) * ((L.d_in + 2047) / 2048);
-        k.rot_items = (L.n_rot < nn ? L.n_rot : nn) * ((L.d_in + 1023) / 1024);
-        k.item0 = item;
-        item += k.copy_items + k.rot_items;
         k.blk0 = blk;
         blk += (long long)k.n_ft * (k.kblocks + k.vkb);
         k.tile0 = tile;

@@ -191,8 +191,7 @@ struct StepCall {
     int tile0;                 // first main tile id
     int lr_rmax;               // largest owned rank (0: no low-rank shrink)
     int out_f32;
-    int copy_items, rot_items, lr_items;
-    int item0;                 // first gather / rotate item
+    int lr_items;              // owned low-rank shrink items
     int lr_item0;              // first low-rank item
 };
 

@@ -86,7 +86,7 @@ struct Ctrl {
     int bad;
     int warp_tot[EPI_WARPS];
     int n_oft[NCALL], n_lrs[NCALL];
-    int done[2][NCALL];   // prologue items this CTA finished per call: token operand, low-rank
+    int done[NCALL];      // low-rank items this CTA finished per call
 };
 constexpr int CTRL_BYTES = 512;
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
@@ -148,20 +148,30 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8]) {
 }
 
 // Bounded wait on an mbarrier phase; gives up when the time limit passes or
-// when this CTA or another one has given up.
+// when this CTA or another one has given up.  The launch-wide abort flag lives
+// in global memory and is read only every few microseconds, so that waiting
+// warps do not keep one L2 line busy; with nap set the warp sleeps between
+// polls (for waits that are not on the streaming path).
 __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                      const int *gabort, bool honour_abort = true) {
+                                      const int *gabort, bool honour_abort = true, bool nap = false) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
+    uint64_t next_global = t0 + 4000;
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (honour_abort && (*abort_flag || *reinterpret_cast<const volatile int *>(gabort))) {
-            *abort_flag = 1;
-            return false;
+        if (nap) __nanosleep(128);
+        if (honour_abort && *abort_flag) return false;
+        const uint64_t now = ptx::globaltimer();
+        if (honour_abort && now > next_global) {
+            if (*reinterpret_cast<const volatile int *>(gabort)) {
+                *abort_flag = 1;
+                return false;
+            }
+            next_global = now + 4000;
         }
-        if (ptx::globaltimer() - t0 > WAIT_NS) {
+        if (now - t0 > WAIT_NS) {
             *abort_flag = 1;
             return false;
         }
@@ -428,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         ctrl->abort = 0;
         ctrl->meta_call = ctrl->v_call = -1;
         ctrl->bad = 0;
-        for (int c = 0; c < NCALL; ++c) ctrl->done[0][c] = ctrl->done[1][c] = 0;
+        for (int c = 0; c < NCALL; ++c) ctrl->done[c] = 0;
         ptx::fence_mbar_init();
     }
     for (int i = threadIdx.x; i <= G; i += THREADS) fx.start[i] = a.start[i];
@@ -464,8 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             };
             auto xs_ready = [&](int c, bool block) -> bool {
                 if ((xs_ok >> c) & 1u) return true;
-                const StepCall &k = a.call[c];
-                const int target = k.copy_items + k.rot_items;
+                const int target = a.grid;   // every CTA adds one per call
                 if (block) {
                     if (!wait_count(sync + SY_XS + c, target, abort_flag, gabort)) return false;
                 } else if (!count_reached(sync + SY_XS + c, target)) {
@@ -728,52 +737,25 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             epi_bar();
         }
 
-        // ---- prologue items
-        float *red = xb;   // shrink reduction scratch
-        // completed items are published once per kind and CTA: every thread's
-        // writes made visible (the token operand is read by TMA, the async
-        // proxy), then one counter add per call
-        auto release_items = [&](int which) {
-            if (which == 0) fence_proxy_async_global();
-            __threadfence();
-            epi_bar();
-            if (et == 0)
-                for (int c = 0; c < a.n_calls; ++c)
-                    if (ctrl->done[which][c]) atomicAdd(sync + (which ? SY_LR : SY_XS) + c, ctrl->done[which][c]);
-        };
-        bool xs_published = false;
-        for (int it = me; it < a.n_items; it += G) {
-            int c = 0, kind = -1, kk = 0;
-            for (int cc = 0; cc < a.n_calls; ++cc) {
-                const StepCall &k = a.call[cc];
-                if (it >= k.item0 && it < k.item0 + k.copy_items + k.rot_items) {
-                    c = cc;
-                    kk = it - k.item0;
-                    kind = kk < k.copy_items ? 0 : 1;
-                    if (kind == 1) kk -= k.copy_items;
-                    break;
-                }
-                if (it >= k.lr_item0 && it < k.lr_item0 + k.lr_items) {
-                    c = cc;
-                    kk = it - k.lr_item0;
-                    kind = 2;
-                    break;
-                }
-            }
-            if (kind < 0) continue;   // uniform across the CTA
-            if (kind == 2 && !xs_published) {
-                release_items(0);
-                xs_published = true;
-            }
-            const StepCall &k = a.call[c];
-            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
-            __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
-            if (kind == 0) {
-                // copy 8 unrotated token rows x 2048 columns
-                const int ccols = (k.d_in + 2047) / 2048;
-                const int rg = kk / ccols, cc = kk - rg * ccols;
-                const int col = cc * 2048 + et * 8;
-                if (col < k.d_in) {
+        // ---- token operands x' of every call, in warp-sized units spread
+        // over all epilogue warps of the launch: copies of 8 unrotated rows x
+        // 256 columns, then rotations of one 32x32 block of one rotated
+        // segment (lane l reads row l of the transposed block; the rows'
+        // inputs arrive by shuffle; the next unit's operands are loaded while
+        // the current one is computed).  Each CTA then adds one per call.
+        {
+            const int W = G * EPI_WARPS, gw = me * EPI_WARPS + ew;
+            int ubase = 0;
+            for (int c = 0; c < a.n_calls; ++c) {
+                const StepCall &k = a.call[c];
+                const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
+                __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
+                const int ccols = (k.d_in + 255) / 256, units = ccols * ((n + 7) / 8);
+#pragma unroll 1
+                for (int u = ((gw - ubase) % W + W) % W; u < units; u += W) {
+                    const int rg = u / ccols, cc = u - rg * ccols;
+                    const int col = cc * 256 + lane * 8;
+                    if (col >= k.d_in) continue;
                     uint4 buf[8];
                     bool live[8];
 #pragma unroll
@@ -788,63 +770,97 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                         if (live[r]) *reinterpret_cast<uint4 *>(xs + (size_t)t * k.kdim + col) = buf[r];
                     }
                 }
-            } else if (kind == 1) {
-                // rotate the rows of one rotated segment over 32 blocks of 32
-                // features: warp ew takes four, one after the other; lane l
-                // produces column l of a block from row l of the transposed
-                // block (four 16-byte loads) and the row's 32 inputs, which
-                // arrive by shuffle.  The next block's operands are loaded
-                // while the current one is computed; the loops stay rolled, so
-                // the code is short.
-                const int ob = (k.d_in + 1023) / 1024;
-                const int s_ord = kk / ob, bg = kk - s_ord * ob;
-                if (s_ord < ctrl->n_oft[c]) {
-                    const int seg = fx.oft_list[c][s_ord];
-                    const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
-                    const __nv_bfloat16 *Rt = fx.segR[c][seg];
-                    const int nblk = k.d_in / OFT_BLK;
-                    const int b0 = bg * 32 + ew * 4;
-                    const int nb = max(0, min(4, nblk - b0));
-                    for (int rb = r0; rb < r1; rb += 4) {
-                        const int nr = min(4, r1 - rb);
-                        uint4 rq[4];
-                        float xv[4];
-                        auto load = [&](int blk) {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(Rt + (size_t)blk * OFT_BLK * OFT_BLK + lane * OFT_BLK);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) rq[u] = src[u];
-#pragma unroll
-                            for (int rr = 0; rr < 4; ++rr)
-                                xv[rr] = rr < nr ? __bfloat162float(x[(size_t)fx.perm[rb + rr] * k.d_in + blk * OFT_BLK + lane]) : 0.f;
-                        };
-                        if (nb > 0) load(b0);
+                ubase += units;
+            }
+            // rotation units of every call, one sequence in call order; a warp
+            // takes four of its units at a time (whichever calls they belong
+            // to) and issues every load of the four before computing any
+            int rbase[NCALL + 1];
+            rbase[0] = 0;
+            for (int c = 0; c < NCALL; ++c)
+                rbase[c + 1] = rbase[c] + (c < a.n_calls ? ctrl->n_oft[c] * (a.call[c].d_in / OFT_BLK) : 0);
+            const int rtot = rbase[NCALL];
 #pragma unroll 1
-                        for (int i = 0; i < nb; ++i) {
-                            float rc[OFT_BLK];
+            for (int g0 = gw; g0 < rtot; g0 += 4 * W) {
+                uint4 rq[4][4];
+                float xv[4][4];
+                int blk[4], r0[4], r1[4], ci[4];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                float f8[8];
-                                unpack8(rq[u], f8);
+                for (int i = 0; i < 4; ++i) {
+                    const int g = g0 + i * W;
+                    r0[i] = r1[i] = blk[i] = ci[i] = 0;
+                    if (g < rtot) {
+                        int c = 0;
+                        while (g >= rbase[c + 1]) ++c;
+                        ci[i] = c;
+                        const int nblk = a.call[c].d_in / OFT_BLK;
+                        const int uu = g - rbase[c], s_ord = uu / nblk;
+                        blk[i] = uu - s_ord * nblk;
+                        const int seg = fx.oft_list[c][s_ord];
+                        r0[i] = fx.seg_start[seg];
+                        r1[i] = fx.seg_start[seg + 1];
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            fx.segR[c][seg] + (size_t)blk[i] * OFT_BLK * OFT_BLK + lane * OFT_BLK);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) rc[u * 8 + e] = f8[e];
-                            }
-                            float xc[4];
+                        for (int q = 0; q < 4; ++q) rq[i][q] = src[q];
+                    }
+                    const StepCall &k = a.call[ci[i]];
+                    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
 #pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) xc[rr] = xv[rr];
-                            if (i + 1 < nb) load(b0 + i + 1);
-                            const int blk = b0 + i;
+                    for (int rr = 0; rr < 4; ++rr)
+                        xv[i][rr] = r0[i] + rr < r1[i]
+                                        ? __bfloat162float(x[(size_t)fx.perm[r0[i] + rr] * k.d_in + blk[i] * OFT_BLK + lane])
+                                        : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (r0[i] >= r1[i]) continue;   // uniform across the warp
+                    const StepCall &k = a.call[ci[i]];
+                    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
+                    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
+                    float rc[OFT_BLK];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float f8[8];
+                        unpack8(rq[i][q], f8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) rc[q * 8 + e] = f8[e];
+                    }
 #pragma unroll 1
-                            for (int rr = 0; rr < nr; ++rr) {
-                                const float xr = rr == 0 ? xc[0] : rr == 1 ? xc[1] : rr == 2 ? xc[2] : xc[3];
-                                float acc = 0.f;
+                    for (int r = r0[i]; r < r1[i]; ++r) {
+                        const int rr = r - r0[i];
+                        const float xr = rr == 0 ? xv[i][0] : rr == 1 ? xv[i][1] : rr == 2 ? xv[i][2] : rr == 3 ? xv[i][3]
+                                       : __bfloat162float(x[(size_t)fx.perm[r] * k.d_in + blk[i] * OFT_BLK + lane]);
+                        float acc = 0.f;
 #pragma unroll
-                                for (int m = 0; m < OFT_BLK; ++m) acc = fmaf(__shfl_sync(0xffffffffu, xr, m), rc[m], acc);
-                                xs[(size_t)fx.perm[rb + rr] * k.kdim + blk * OFT_BLK + lane] = __float2bfloat16_rn(acc);
-                            }
-                        }
+                        for (int m = 0; m < OFT_BLK; ++m) acc = fmaf(__shfl_sync(0xffffffffu, xr, m), rc[m], acc);
+                        xs[(size_t)fx.perm[r] * k.kdim + blk[i] * OFT_BLK + lane] = __float2bfloat16_rn(acc);
                     }
                 }
-            } else {
+            }
+            fence_proxy_async_global();
+            __threadfence();
+            epi_bar();
+            if (et == 0)
+                for (int c = 0; c < a.n_calls; ++c) atomicAdd(sync + SY_XS + c, 1);
+        }
+
+        // ---- owned low-rank shrink items (CTA-sized)
+        float *red = xb;   // shrink reduction scratch
+        for (int it = me; it < a.n_items; it += G) {
+            int c = 0, kk = -1;
+            for (int cc = 0; cc < a.n_calls; ++cc) {
+                const StepCall &k = a.call[cc];
+                if (it >= k.lr_item0 && it < k.lr_item0 + k.lr_items) {
+                    c = cc;
+                    kk = it - k.lr_item0;
+                    break;
+                }
+            }
+            if (kk < 0) continue;   // uniform across the CTA
+            const StepCall &k = a.call[c];
+            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
+            {
                 // owned low-rank shrink: LR_Q ranks of one segment
                 const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
                 const int s_ord = kk / ng, qg = kk - s_ord * ng;
@@ -861,10 +877,15 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     }
                 }
             }
-            if (et == 0) ++ctrl->done[kind == 2 ? 1 : 0][c];
+            if (et == 0) ++ctrl->done[c];
         }
-        if (!xs_published) release_items(0);
-        release_items(1);
+        // completed low-rank items are published once per CTA: every thread's
+        // writes made visible, then one counter add per call
+        __threadfence();
+        epi_bar();
+        if (et == 0)
+            for (int c = 0; c < a.n_calls; ++c)
+                if (ctrl->done[c]) atomicAdd(sync + SY_LR + c, ctrl->done[c]);
         epi_bar();
 
         // ---- epilogues, one per segment of this CTA's work, in issue order
@@ -876,7 +897,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         for (int u = me; ok && u < a.n_units; u += G) {
             const ULoc U = ulocate(a, u);
             const StepCall &k = a.call[U.c];
-            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort)) { ok = false; break; }
+            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
             const int nctr = k.vs_chunks;
@@ -956,7 +977,27 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             const MLoc L = mlocate(a, b);
             const StepCall &k = a.call[L.c];
             const long long se = min(mend, L.tb0 + L.nkb);
-            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort)) { ok = false; break; }
+            if (se == mend) {
+                // this CTA's last segment: it most likely arrives last at this
+                // tile, and that epilogue is the launch's tail, so while the K
+                // loop runs L2 is asked for what the epilogue reads
+                stage_meta(a, L.c, fx, ctrl, et);
+                const int f0 = L.tile * TILE_M;
+                for (int e = et; e < n * 16; e += EPI_THREADS) {
+                    const int t = e >> 4, j = e & 15;
+                    const TokMeta &m = fx.tmeta[t];
+                    if (j < 4) {
+                        if (m.s) ptx::prefetch_l2(m.s + f0 + j * 32);
+                        if (m.b) ptx::prefetch_l2(m.b + f0 + j * 32);
+                        if (m.ve) ptx::prefetch_l2(m.ve + f0 + j * 32);
+                    }
+                    for (int q = j; q < m.rank; q += 16) {
+                        ptx::prefetch_l2(m.B + (size_t)q * k.d_out + f0);
+                        ptx::prefetch_l2(m.B + (size_t)q * k.d_out + f0 + 64);
+                    }
+                }
+            }
+            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
             // contributors: the CTAs between the owners of the tile's first and
