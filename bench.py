@@ -78,6 +78,16 @@ def parse():
     return p.parse_args()
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a few host floats over every rank of the
+    default process group (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
@@ -334,9 +344,7 @@ def main():
     ms = float(np.mean(t_mixed))
     ms_lora = float(np.mean(t_lora))
     if world > 1:
-        tt = torch.tensor([ms, ms_lora], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, ms_lora = float(tt[0]), float(tt[1])
+        ms, ms_lora = max_over_ranks([ms, ms_lora], dev)
 
     # byte model of the step: the one launch moves every projection's bytes
     bm = {p: ctx.predict_bytes(w.ids, ctx.layer_ids[p], "bf16") for p in PROJ}
@@ -367,9 +375,7 @@ def main():
             e2e_t.append(e0.elapsed_time(e1))
     e2e_ms = float(np.mean(e2e_t))
     if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt[0])
+        (e2e_ms,) = max_over_ranks([e2e_ms], dev)
     if ctx.sync_status() != 0:
         raise RuntimeError("device status error after the timed region")
 
