@@ -349,6 +349,15 @@ scute_status scute_timing_enable(scute_ctx *ctx, int enable);
 scute_status scute_timing_reset(scute_ctx *ctx);
 scute_status scute_timing_read(scute_ctx *ctx, float *ms_out, int max, int *n_out);
 
+/* Test hook for the failure path (no counterpart in the article).  With
+ * what = SCUTE_INJECT_STALL, the context's next decode launch (bf16, n <= 128)
+ * waits for a count that no CTA ever reaches: its bounded waits run out (about
+ * 2 s), every CTA drains what it issued, frees TMEM and returns, and
+ * scute_sync_status then reports SCUTE_ERR_TIMEOUT.  The context stays usable;
+ * the hook applies to that one launch only.  Nothing traps or faults. */
+#define SCUTE_INJECT_STALL 1
+scute_status scute_debug_inject(scute_ctx *ctx, int what);
+
 #ifdef __cplusplus
 }
 #endif

@@ -111,6 +111,7 @@ _SIGS = {
     "scute_launch_count": (ctypes.c_int64, [ctypes.c_void_p]),
     "scute_timing_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_timing_reset": (ctypes.c_int, [ctypes.c_void_p]),
+    "scute_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]),
 }
@@ -290,6 +291,13 @@ def scute_timing_enable(ctx, enable: bool):
 
 def scute_timing_reset(ctx):
     _check(ctx, load().scute_timing_reset(ctx))
+
+
+INJECT_STALL = 1
+
+
+def scute_debug_inject(ctx, what: int) -> None:
+    _check(ctx, load().scute_debug_inject(ctx, what))
 
 
 def scute_timing_read(ctx, max_slots: int = TIMING_SLOTS) -> list:

@@ -642,6 +642,8 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
     a.n_tiles = tile;
     a.n_items = item;
     a.rmax = rmax;
+    a.hold = c->inject == SCUTE_INJECT_STALL ? 1 : 0;
+    c->inject = 0;
     int S = 8;
     while (S > 2 && step_smem_bytes(BN, S, rmax) > (size_t)c->smem_optin) --S;
     if (step_smem_bytes(BN, S, rmax) > (size_t)c->smem_optin)
@@ -969,6 +971,13 @@ scute_status scute_timing_reset(scute_ctx *c) {
     if (!c) return SCUTE_ERR_ARG;
     c->t_next = 0;
     c->t_used = 0;
+    return SCUTE_OK;
+}
+
+scute_status scute_debug_inject(scute_ctx *c, int what) {
+    if (!c) return SCUTE_ERR_ARG;
+    if (what != 0 && what != SCUTE_INJECT_STALL) return fail(c, SCUTE_ERR_ARG, "unknown injection %d", what);
+    c->inject = what;
     return SCUTE_OK;
 }
 

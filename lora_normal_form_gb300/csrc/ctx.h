@@ -89,6 +89,7 @@ struct scute_ctx {
     size_t step_hout_cols = 0;
     int step_bn_max = 64;
     int smem_optin = 0;
+    int inject = 0;              // scute_debug_inject, consumed by the next decode launch
     PFN_encodeTiled encode = nullptr;
     int64_t launches = 0;
     bool timing = false;

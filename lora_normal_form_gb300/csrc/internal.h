@@ -210,6 +210,7 @@ struct StepArgs {
     int n_tiles;               // main tiles over all calls
     int n_items;               // prologue items over all calls
     int rmax;                  // largest lr_rmax (shared-memory v rows)
+    int hold;                  // extra count the token-operand wait needs (failure-path test)
     long long start[STEP_MAX_GRID + 1];   // main-block range of each CTA: [start[i], start[i+1])
 };
 

@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             };
             auto xs_ready = [&](int c, bool block) -> bool {
                 if ((xs_ok >> c) & 1u) return true;
-                const int target = a.grid;   // every CTA adds one per call
+                const int target = a.grid + a.hold;   // every CTA adds one per call
                 if (block) {
                     if (!wait_count(sync + SY_XS + c, target, abort_flag, gabort)) return false;
                 } else if (!count_reached(sync + SY_XS + c, target)) {
