@@ -329,6 +329,66 @@ __device__ __forceinline__ void add_part(const float *src, float (&acc)[8]) {
     acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
 }
 
+// b + v B' of a tile this CTA finishes, in a call with owned low-rank terms,
+// formed while the K loop streams, in this CTA's own slot of the tile (each
+// thread later reads back only what it wrote).  Takes the segment that starts
+// at stream block b0 (ranges end at mend); returns where it ends, or -1 when a
+// wait gave up.  All epilogue threads call it.
+__device__ __noinline__ long long form_pre(const StepArgs &a, Fixed &fx, Ctrl *ctrl, float *vsm, long long b0,
+                                           long long mend, int me, int et, volatile int *abort_flag,
+                                           const int *gabort) {
+    const MLoc L = mlocate(a, b0);
+    const StepCall &k = a.call[L.c];
+    const long long se = min(mend, L.tb0 + L.nkb);
+    if (b0 != L.tb0 || k.lr_rmax == 0) return se;
+    const int n = a.n;
+    if (ctrl->v_call != L.c) {
+        epi_bar();
+        if (et == 0) ctrl->flag = wait_count(a.sync + SY_LR + L.c, k.lr_items, abort_flag, gabort) ? 1 : 0;
+        epi_bar();
+        if (!ctrl->flag) return -1;
+        for (int e = et; e < n * k.lr_rmax; e += EPI_THREADS) {
+            const int t = e / k.lr_rmax, q = e - t * k.lr_rmax;
+            vsm[t * a.rmax + q] = __ldcg(k.v + (size_t)t * MAX_RANK + q);
+        }
+        epi_bar();
+        if (et == 0) ctrl->v_call = L.c;
+    }
+    stage_meta(a, L.c, fx, ctrl, et);
+    const int f0 = L.tile * TILE_M;
+    float *own = a.part + (size_t)(a.n_units + k.tile0 + L.tile + me) * ((size_t)2 * TILE_M * a.bn);
+#pragma unroll 1
+    for (int it = et; it < n * 16; it += EPI_THREADS) {
+        const int t = it >> 4, j0 = f0 + (it & 15) * 8;
+        if (j0 >= k.d_out) continue;
+        const TokMeta &m = fx.tmeta[t];
+        float y[8];
+        ld_vec8(m.b + j0, m.b != nullptr, 0.f, y);
+        const float *vrow = vsm + t * a.rmax;
+#pragma unroll 1
+        for (int q0 = 0; q0 < m.rank; q0 += 16) {
+            uint4 bq[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)(q0 + q) * k.d_out));
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                if (q0 + q < m.rank) {
+                    float bf[8];
+                    unpack8(bq[q], bf);
+                    const float vq = vrow[q0 + q];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
+                }
+            }
+        }
+        float4 *dp = reinterpret_cast<float4 *>(own + (size_t)t * TILE_M + (it & 15) * 8);
+        dp[0] = make_float4(y[0], y[1], y[2], y[3]);
+        dp[1] = make_float4(y[4], y[5], y[6], y[7]);
+    }
+    return se;
+}
+
 // x_i A_rows^T for up to LR_Q rows of A (each [d_in], bf16) and the sorted
 // rows [r0, r1) (tokens perm[r]); emit(token, q, value) once per (row, q).
 // Each of the 256 threads covers 8 consecutive k per pass; a warp reduces its
@@ -462,6 +522,9 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
+            // every weight box is read by exactly one CTA once: let it leave L2
+            // first, ahead of the token operands, slots and partial tiles
+            const uint64_t once = ptx::make_policy_evict_first();
             unsigned xs_ok = 0, u_ok = 0;
             bool ok = true;
             // stages whose weight boxes are issued but whose token-operand
@@ -514,8 +577,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 const uint32_t sP = ptx::smem_u32(sbase + stage * STAGE);
                 const uint32_t sQ = sP + P_BYTES;
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
-                ptx::tma_load_2d(sP, mp, kc, prow, fb);
-                ptx::tma_load_2d(sP + BOX_BYTES, mp, kc, prow + BOX_ROWS, fb);
+                ptx::tma_load_2d_hint(sP, mp, kc, prow, fb, once);
+                ptx::tma_load_2d_hint(sP + BOX_BYTES, mp, kc, prow + BOX_ROWS, fb, once);
                 if (!xs_dep) {
                     issue_q(sQ, fb, mq, kc);
                 } else {
@@ -973,73 +1036,96 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
             if (++buf == 2) { buf = 0; bph ^= 1; }
         }
+        long long pre_to = ms;   // segments that start before pre_to have their b + v B'
         for (long long b = ms; ok && b < mend;) {
             const MLoc L = mlocate(a, b);
             const StepCall &k = a.call[L.c];
             const long long se = min(mend, L.tb0 + L.nkb);
-            if (se == mend) {
-                // this CTA's last segment: it most likely arrives last at this
-                // tile, and that epilogue is the launch's tail, so while the K
-                // loop runs L2 is asked for what the epilogue reads
-                stage_meta(a, L.c, fx, ctrl, et);
-                const int f0 = L.tile * TILE_M;
-                for (int e = et; e < n * 16; e += EPI_THREADS) {
-                    const int t = e >> 4, j = e & 15;
-                    const TokMeta &m = fx.tmeta[t];
-                    if (j < 4) {
-                        if (m.s) ptx::prefetch_l2(m.s + f0 + j * 32);
-                        if (m.b) ptx::prefetch_l2(m.b + f0 + j * 32);
-                        if (m.ve) ptx::prefetch_l2(m.ve + f0 + j * 32);
-                    }
-                    for (int q = j; q < m.rank; q += 16) {
-                        ptx::prefetch_l2(m.B + (size_t)q * k.d_out + f0);
-                        ptx::prefetch_l2(m.B + (size_t)q * k.d_out + f0 + 64);
-                    }
-                }
+            const int gtile = k.tile0 + L.tile;
+            const int f0 = L.tile * TILE_M;
+            // The CTA that holds a tile's first block finishes the tile.  It
+            // reaches that tile at the end of its range, while the CTAs that
+            // share the tile hold it at the start of theirs and publish their
+            // partial sums early; waits therefore only run from a CTA to
+            // higher-numbered ones, and nothing waits in a cycle.
+            const bool fin = b == L.tb0;
+            float *own = a.part + (size_t)(a.n_units + gtile + me) * SLOT;
+            // b + v B' for this segment's tile and the next one's: the next
+            // tile's is ready before its (possibly short) K loop ends
+            while (ok && pre_to < mend && pre_to <= se) {
+                pre_to = form_pre(a, fx, ctrl, vsm, pre_to, mend, me, et, abort_flag, gabort);
+                if (pre_to < 0) ok = false;
             }
+            if (!ok) break;
+            const int lastc = fin ? owner(fx, G, L.tb0 + L.nkb - 1) : me;
             if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
-            // contributors: the CTAs between the owners of the tile's first and
-            // last block whose ranges are not empty
-            const int first = owner(fx, G, L.tb0), lastc = owner(fx, G, L.tb0 + L.nkb - 1);
-            int nctr = 0;
-            for (int j = first; j <= lastc; ++j) nctr += fx.start[j + 1] > fx.start[j] ? 1 : 0;
-            const bool my_m = b - L.tb0 < k.kblocks;
             const bool my_v = k.vkb > 0 && se - L.tb0 > k.kblocks;
-            const int gtile = k.tile0 + L.tile;
-            bool last = true;
-            if (nctr > 1) {
-                float *dst = a.part + (size_t)(a.n_units + gtile + me) * SLOT;
-                if (my_m) publish(tcol, dst, n, BN, row, half);
-                if (my_v) publish(tcol + BN, dst + (size_t)TILE_M * BN, n, BN, row, half);
-                last = arrive(sync + SY_TILE + gtile, nctr, ctrl, et);
-            }
-            if (last) {
-                if (k.lr_rmax > 0 && ctrl->v_call != L.c) {
+            if (!fin) {
+                // hand this CTA's part of the tile to the tile's finisher
+                if (b - L.tb0 < k.kblocks) publish(tcol, own, n, BN, row, half);
+                if (my_v) publish(tcol + BN, own + (size_t)TILE_M * BN, n, BN, row, half);
+                __threadfence();
+                epi_bar();
+                if (et == 0) atomicAdd(sync + SY_TILE + gtile, 1);
+            } else {
+                int others = 0;
+                for (int j = me + 1; j <= lastc; ++j) others += fx.start[j + 1] > fx.start[j] ? 1 : 0;
+                if (others > 0) {
                     epi_bar();
-                    if (et == 0) ctrl->flag = wait_count(sync + SY_LR + L.c, k.lr_items, abort_flag, gabort) ? 1 : 0;
-                    epi_bar();
-                    if (!ctrl->flag) ok = false;
-                    if (ok) {
-                        for (int e = et; e < n * k.lr_rmax; e += EPI_THREADS) {
-                            const int t = e / k.lr_rmax, q = e - t * k.lr_rmax;
-                            vsm[t * a.rmax + q] = __ldcg(k.v + (size_t)t * MAX_RANK + q);
-                        }
-                        if (et == 0) ctrl->v_call = L.c;
+                    if (et == 0) {
+                        ctrl->flag = wait_count(sync + SY_TILE + gtile, others, abort_flag, gabort) ? 1 : 0;
                     }
                     epi_bar();
+                    if (!ctrl->flag) ok = false;
+                    __threadfence();
                 }
                 if (ok) {
                     stage_meta(a, L.c, fx, ctrl, et);
-                    const int f0 = L.tile * TILE_M;
                     for (int c32 = 0; c32 * 32 < n; ++c32) {
-                        // a lone contributor's tile comes from TMEM (half 0 drains
-                        // the base accumulator, half 1 the VeRA one); otherwise
-                        // every published partial is summed in CTA order, this
-                        // CTA's too, so the result does not depend on which CTA
-                        // finished last
-                        if (nctr == 1 && (half == 0 || k.vkb > 0)) {
+                        // operands first: none of them depends on the accumulator
+                        float s8[2][8], e8[2][8], p8[2][8], oth[2][8], voth[2][8];
+                        int t[2], g[2];
+                        bool live[2];
+#pragma unroll
+                        for (int p = 0; p < 2; ++p) {
+                            const int it = c32 * 2 * EPI_THREADS + p * EPI_THREADS + et;
+                            t[p] = it >> 4;
+                            g[p] = it & 15;
+                            const int j0 = f0 + g[p] * 8;
+                            live[p] = t[p] < n && j0 < k.d_out;
+                            const TokMeta &m = fx.tmeta[live[p] ? t[p] : 0];
+                            ld_vec8(m.s + j0, live[p] && m.s != nullptr, 1.f, s8[p]);
+                            ld_vec8(m.ve + j0, live[p] && m.vera && m.ve != nullptr, 0.f, e8[p]);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) { oth[p][e] = 0.f; voth[p][e] = 0.f; }
+                            if (k.lr_rmax == 0) {
+                                ld_vec8(m.b + j0, live[p] && m.b != nullptr, 0.f, p8[p]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) p8[p][e] = 0.f;
+                                if (live[p]) add_part(own + (size_t)t[p] * TILE_M + g[p] * 8, p8[p]);   // written by this thread
+                            }
+                        }
+                        // the sharers' partial tiles, in CTA order
+#pragma unroll 1
+                        for (int j = me + 1; j <= lastc; ++j) {
+                            if (fx.start[j + 1] <= fx.start[j]) continue;
+                            const long long lo = max(L.tb0, fx.start[j]), hi = min(L.tb0 + L.nkb, fx.start[j + 1]);
+                            const bool om = lo - L.tb0 < k.kblocks, ov = k.vkb > 0 && hi - L.tb0 > k.kblocks;
+                            const float *sp = a.part + (size_t)(a.n_units + gtile + j) * SLOT;
+#pragma unroll
+                            for (int p = 0; p < 2; ++p) {
+                                if (!live[p]) continue;
+                                const float *q = sp + (size_t)t[p] * TILE_M + g[p] * 8;
+                                if (om) add_part(q, oth[p]);
+                                if (ov) add_part(q + (size_t)TILE_M * BN, voth[p]);
+                            }
+                        }
+                        // this CTA's own sums come from TMEM: half 0 drains the
+                        // base accumulator, half 1 the VeRA one
+                        if (half == 0 || my_v) {
                             float *dstp = half == 0 ? xbm : xbv;
                             float v[32];
                             ptx::tmem_ld32(tcol + (half ? BN : 0) + c32 * 32, v);
@@ -1047,96 +1133,20 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                             for (int kk = 0; kk < 32; ++kk) dstp[kk * RED + row] = v[kk];
                         }
                         epi_bar();
-#pragma unroll 1
+#pragma unroll
                         for (int p = 0; p < 2; ++p) {
-                            const int it = et + p * EPI_THREADS;
-                            const int kk = it >> 4, g = it & 15;
-                            const int t = c32 * 32 + kk, j0 = f0 + g * 8;
-                            if (t >= n || j0 >= k.d_out) continue;
-                            const TokMeta &m = fx.tmeta[t];
-                            // the slot operands do not depend on the sums: ask for them first
-                            float s8[8], b8[8], e8[8];
-                            ld_vec8(m.s + j0, m.s != nullptr, 1.f, s8);
-                            ld_vec8(m.b + j0, m.b != nullptr, 0.f, b8);
-                            ld_vec8(m.ve + j0, m.ve != nullptr, 1.f, e8);
-                            uint4 bq[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                if (q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)q * k.d_out));
-                            float acc[8], vacc[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                acc[e] = nctr == 1 ? xbm[kk * RED + g * 8 + e] : 0.f;
-                                vacc[e] = (nctr == 1 && k.vkb > 0) ? xbv[kk * RED + g * 8 + e] : 0.f;
-                            }
-                            // the contributors' partial tiles, two at a time, in CTA order
-                            for (int jb = first; nctr > 1 && jb <= lastc; jb += 2) {
-                                float4 pm[2][2], pv[2][2];
-                                bool om[2], ov[2];
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const int j = jb + u;
-                                    const bool valid = j <= lastc && fx.start[j + 1] > fx.start[j];
-                                    const long long lo = valid ? max(L.tb0, fx.start[j]) : 0;
-                                    const long long hi = valid ? min(L.tb0 + L.nkb, fx.start[j + 1]) : 0;
-                                    om[u] = valid && lo - L.tb0 < k.kblocks;
-                                    ov[u] = valid && k.vkb > 0 && hi - L.tb0 > k.kblocks;
-                                    const float *sp = a.part + (size_t)(a.n_units + gtile + j) * SLOT + (size_t)t * TILE_M + g * 8;
-                                    if (om[u]) {
-                                        pm[u][0] = __ldcg(reinterpret_cast<const float4 *>(sp));
-                                        pm[u][1] = __ldcg(reinterpret_cast<const float4 *>(sp + 4));
-                                    }
-                                    if (ov[u]) {
-                                        pv[u][0] = __ldcg(reinterpret_cast<const float4 *>(sp + (size_t)TILE_M * BN));
-                                        pv[u][1] = __ldcg(reinterpret_cast<const float4 *>(sp + (size_t)TILE_M * BN + 4));
-                                    }
-                                }
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    if (om[u]) {
-                                        acc[0] += pm[u][0].x; acc[1] += pm[u][0].y; acc[2] += pm[u][0].z; acc[3] += pm[u][0].w;
-                                        acc[4] += pm[u][1].x; acc[5] += pm[u][1].y; acc[6] += pm[u][1].z; acc[7] += pm[u][1].w;
-                                    }
-                                    if (ov[u]) {
-                                        vacc[0] += pv[u][0].x; vacc[1] += pv[u][0].y; vacc[2] += pv[u][0].z; vacc[3] += pv[u][0].w;
-                                        vacc[4] += pv[u][1].x; vacc[5] += pv[u][1].y; vacc[6] += pv[u][1].z; vacc[7] += pv[u][1].w;
-                                    }
-                                }
-                            }
-                            // y = acc * s + b + v B'[:, j0:j0+8] + vacc * e
-                            const float *vrow = vsm + t * a.rmax;
-                            const float vs = m.vera ? 1.f : 0.f;
+                            if (!live[p]) continue;
+                            const int kk = t[p] - c32 * 32, j0 = f0 + g[p] * 8;
+                            // y = acc s + (b + v B') + vacc e
                             float y[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) y[e] = fmaf(acc[e], s8[e], b8[e]) + vs * vacc[e] * e8[e];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                if (q < m.rank) {
-                                    float bf[8];
-                                    unpack8(bq[q], bf);
-                                    const float vq = vrow[q];
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
-                                }
-                            }
-#pragma unroll 1
-                            for (int q0 = 8; q0 < m.rank; q0 += 8) {
-#pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)(q0 + q) * k.d_out));
-#pragma unroll
-                                for (int q = 0; q < 8; ++q) {
-                                    if (q0 + q < m.rank) {
-                                        float bf[8];
-                                        unpack8(bq[q], bf);
-                                        const float vq = vrow[q0 + q];
-#pragma unroll
-                                        for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
-                                    }
-                                }
+                            for (int e = 0; e < 8; ++e) {
+                                const float acc = xbm[kk * RED + g[p] * 8 + e] + oth[p][e];
+                                const float vacc = (my_v ? xbv[kk * RED + g[p] * 8 + e] : 0.f) + voth[p][e];
+                                y[e] = fmaf(vacc, e8[p][e], fmaf(acc, s8[p][e], p8[p][e]));
                             }
                             if (k.out_f32) {
-                                float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(k.out) + (size_t)t * k.d_out + j0);
+                                float4 *o = reinterpret_cast<float4 *>(reinterpret_cast<float *>(k.out) + (size_t)t[p] * k.d_out + j0);
                                 o[0] = make_float4(y[0], y[1], y[2], y[3]);
                                 o[1] = make_float4(y[4], y[5], y[6], y[7]);
                             } else {
@@ -1144,12 +1154,29 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                                 __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(y[2 * e], y[2 * e + 1]);
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(k.out) + (size_t)t * k.d_out + j0) = pk;
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(k.out) + (size_t)t[p] * k.d_out + j0) = pk;
                             }
                         }
                         epi_bar();
+                        // the slot rows of this chunk are not read again: drop
+                        // them from L2 without writing them back (threads below
+                        // 128 take the base planes, the others the VeRA planes)
+                        const int tl = c32 * 32 + ((et & 127) >> 2);
+                        if (tl < n) {
+                            const size_t off = (size_t)tl * TILE_M + (et & 3) * 32 + (et < 128 ? 0 : (size_t)TILE_M * BN);
+                            if (et < 128 && k.lr_rmax > 0) ptx::discard_l2(own + off);
+#pragma unroll 1
+                            for (int j = me + 1; j <= lastc; ++j) {
+                                if (fx.start[j + 1] <= fx.start[j]) continue;
+                                const long long lo = max(L.tb0, fx.start[j]), hi = min(L.tb0 + L.nkb, fx.start[j + 1]);
+                                const bool om = lo - L.tb0 < k.kblocks, ov = k.vkb > 0 && hi - L.tb0 > k.kblocks;
+                                if (et < 128 ? om : ov) ptx::discard_l2(a.part + (size_t)(a.n_units + gtile + j) * SLOT + off);
+                            }
+                        }
                     }
                 }
+                // every sharer has counted: clear the tile's counter for the next launch
+                if (others > 0 && ok && et == 0) sync[SY_TILE + gtile] = 0;
             }
             ptx::tc_fence_before();
             __syncwarp();
