@@ -565,6 +565,13 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
             k.mapBsh = L.mapBsh;
             if (!encode_map(c, &k.mapU, k.U, (uint64_t)L.krv, (uint64_t)STEP_MAX_TOKENS))
                 return fail(c, SCUTE_ERR_CUDA, "tensor map for the VeRA intermediate failed");
+            // VeRA tokens are never rotated, so their rows of x' are rows of x:
+            // the shrink may read x directly and start before x' is formed
+            // (rows of other tokens are discarded by the shrink's epilogue)
+            k.vs_x = (reinterpret_cast<uintptr_t>(k.x) % 16 == 0 && ((size_t)L.d_in * c->esz) % 16 == 0 &&
+                      encode_map(c, &k.mapX, k.x, (uint64_t)L.d_in, (uint64_t)nn))
+                         ? 1
+                         : 0;
         }
         k.d_in = L.d_in;
         k.kdim = L.kdim;

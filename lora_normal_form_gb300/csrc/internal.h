@@ -173,6 +173,7 @@ struct StepCall {
     CUtensorMap mapAsh;        // A_sh^T [rv][kdim]
     CUtensorMap mapBsh;        // B_sh^T [d_out][krv]
     CUtensorMap mapU;          // VeRA intermediate [128][krv]
+    CUtensorMap mapX;          // caller input [n][d_in] (VeRA shrink operand when vs_x)
     const void *x;             // [n][d_in] caller input
     void *xs;                  // [128][kdim]
     void *U;                   // [128][krv]
@@ -193,6 +194,7 @@ struct StepCall {
     int out_f32;
     int lr_items;              // owned low-rank shrink items
     int lr_item0;              // first low-rank item
+    int vs_x;                  // VeRA shrink reads x itself (no wait for x')
 };
 
 struct StepArgs {

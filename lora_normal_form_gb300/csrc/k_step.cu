@@ -116,6 +116,19 @@ struct Fixed {
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier as a vote: true when v holds in all 256 epilogue threads.
+// A wait that some warps see end and others see give up must not split them
+// (the split would leave both halves at different barriers for good), so the
+// epilogue acts on the vote of every such wait.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -351,8 +364,8 @@ __device__ __noinline__ long long form_pre(const StepArgs &a, Fixed &fx, Ctrl *c
             const int t = e / k.lr_rmax, q = e - t * k.lr_rmax;
             vsm[t * a.rmax + q] = __ldcg(k.v + (size_t)t * MAX_RANK + q);
         }
+        if (et == 0) ctrl->v_call = L.c;   // read again only after the barrier below
         epi_bar();
-        if (et == 0) ctrl->v_call = L.c;
     }
     stage_meta(a, L.c, fx, ctrl, et);
     const int f0 = L.tile * TILE_M;
@@ -518,6 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             for (int c = 0; c < a.n_calls; ++c) {
                 ptx::prefetch_tmap(&a.call[c].mapW);
                 ptx::prefetch_tmap(&a.call[c].mapXs);
+                if (a.call[c].vs_x) ptx::prefetch_tmap(&a.call[c].mapX);
             }
             int stage = 0;
             uint32_t phase = 0;
@@ -602,7 +616,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 const ULoc U = ulocate(a, u);
                 const StepCall &k = a.call[U.c];
                 for (int kb = U.kb0; ok && kb < U.kb1; ++kb)
-                    ok = issue(&k.mapAsh, U.vt * TILE_M, &k.mapXs, kb * 64, U.c, true);
+                    ok = k.vs_x ? issue(&k.mapAsh, U.vt * TILE_M, &k.mapX, kb * 64, U.c, false)
+                                : issue(&k.mapAsh, U.vt * TILE_M, &k.mapXs, kb * 64, U.c, true);
             }
             for (long long b = ms; ok && b < mend;) {
                 const MLoc L = mlocate(a, b);
@@ -800,6 +815,94 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             epi_bar();
         }
 
+        int buf = 0;
+        uint32_t bph = 0;
+        bool ok = true;
+        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);
+        float *xbm = xb, *xbv = xb + 32 * RED;
+        // VeRA shrink unit u (a CTA has at most one; it is the first use of the
+        // TMEM buffers): publish the partial sums, or, arriving last, write U
+        auto unit_epi = [&](int u) -> bool {
+            const ULoc U = ulocate(a, u);
+            const StepCall &k = a.call[U.c];
+            if (!epi_all(wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true))) return false;
+            ptx::tc_fence_after();
+            const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
+            const int nctr = k.vs_chunks;
+            const int u0 = k.vs_unit0 + U.vt * nctr;
+            bool last = true;
+            if (nctr > 1) {
+                publish(tcol, a.part + (size_t)u * SLOT, n, BN, row, half);
+                last = arrive(sync + SY_VTILE + U.c * STEP_MAX_VTILES + U.vt, nctr, ctrl, et);
+            }
+            if (last) {
+                // U[t][q] = (x' A_sh)[t][q] * d_a(t)[q] for VeRA tokens, 0 otherwise
+                stage_meta(a, U.c, fx, ctrl, et);
+                const int r0 = U.vt * TILE_M;
+                __nv_bfloat16 *Ub = reinterpret_cast<__nv_bfloat16 *>(k.U);
+                for (int c32 = 0; c32 * 32 < n; ++c32) {
+                    // a lone contributor's tile comes from TMEM; otherwise every
+                    // published partial is summed in unit order, this CTA's too,
+                    // so the result does not depend on which CTA finished last
+                    if (half == 0 && nctr == 1) {
+                        float v[32];
+                        ptx::tmem_ld32(tcol + c32 * 32, v);
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) xbm[kk * RED + row] = v[kk];
+                    }
+                    epi_bar();
+                    int t[2], q0[2], g[2], kk[2];
+                    bool live[2];
+                    float acc[2][8];
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const int it = et + p * EPI_THREADS;
+                        kk[p] = it >> 4;
+                        g[p] = it & 15;
+                        t[p] = c32 * 32 + kk[p];
+                        q0[p] = r0 + g[p] * 8;
+                        live[p] = t[p] < n && q0[p] < k.krv;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[p][e] = nctr == 1 ? xbm[kk[p] * RED + g[p] * 8 + e] : 0.f;
+                    }
+#pragma unroll 4
+                    for (int j = 0; j < (nctr > 1 ? nctr : 0); ++j) {
+                        const float *src = a.part + (size_t)(u0 + j) * SLOT;
+#pragma unroll
+                        for (int p = 0; p < 2; ++p)
+                            if (live[p]) add_part(src + (size_t)t[p] * TILE_M + g[p] * 8, acc[p]);
+                    }
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        if (!live[p]) continue;
+                        const float *vd = fx.tmeta[t[p]].vd;
+                        uint4 pk;
+                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+                        if (vd && q0[p] < k.rv) {
+                            float d8[8];
+                            ld_vec8(vd + q0[p], true, 0.f, d8);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                p2[e] = __floats2bfloat162_rn(acc[p][2 * e] * d8[2 * e], acc[p][2 * e + 1] * d8[2 * e + 1]);
+                        } else {
+                            pk = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        *reinterpret_cast<uint4 *>(Ub + (size_t)t[p] * k.krv + q0[p]) = pk;
+                    }
+                    epi_bar();
+                }
+                fence_proxy_async_global();
+                __threadfence();
+                epi_bar();
+                if (et == 0) atomicAdd(sync + SY_U + U.c, 1);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
+            if (++buf == 2) { buf = 0; bph ^= 1; }
+            return true;
+        };
+
         // ---- token operands x' of every call, in warp-sized units spread
         // over all epilogue warps of the launch: copies of 8 unrotated rows x
         // 256 columns, then rotations of one 32x32 block of one rotated
@@ -908,6 +1011,10 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 for (int c = 0; c < a.n_calls; ++c) atomicAdd(sync + SY_XS + c, 1);
         }
 
+        // ---- the VeRA shrink unit of this CTA, if any: U is written before
+        // the low-rank items, so that the tiles' VeRA blocks wait little
+        for (int u = me; ok && u < a.n_units; u += G) ok = unit_epi(u);
+
         // ---- owned low-rank shrink items (CTA-sized)
         float *red = xb;   // shrink reduction scratch
         for (int it = me; it < a.n_items; it += G) {
@@ -952,90 +1059,6 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         epi_bar();
 
         // ---- epilogues, one per segment of this CTA's work, in issue order
-        int buf = 0;
-        uint32_t bph = 0;
-        bool ok = true;
-        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);
-        float *xbm = xb, *xbv = xb + 32 * RED;
-        for (int u = me; ok && u < a.n_units; u += G) {
-            const ULoc U = ulocate(a, u);
-            const StepCall &k = a.call[U.c];
-            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
-            const int nctr = k.vs_chunks;
-            const int u0 = k.vs_unit0 + U.vt * nctr;
-            bool last = true;
-            if (nctr > 1) {
-                publish(tcol, a.part + (size_t)u * SLOT, n, BN, row, half);
-                last = arrive(sync + SY_VTILE + U.c * STEP_MAX_VTILES + U.vt, nctr, ctrl, et);
-            }
-            if (last) {
-                // U[t][q] = (x' A_sh)[t][q] * d_a(t)[q] for VeRA tokens, 0 otherwise
-                stage_meta(a, U.c, fx, ctrl, et);
-                const int r0 = U.vt * TILE_M;
-                __nv_bfloat16 *Ub = reinterpret_cast<__nv_bfloat16 *>(k.U);
-                for (int c32 = 0; c32 * 32 < n; ++c32) {
-                    // a lone contributor's tile comes from TMEM; otherwise every
-                    // published partial is summed in unit order, this CTA's too,
-                    // so the result does not depend on which CTA finished last
-                    if (half == 0 && nctr == 1) {
-                        float v[32];
-                        ptx::tmem_ld32(tcol + c32 * 32, v);
-#pragma unroll
-                        for (int kk = 0; kk < 32; ++kk) xbm[kk * RED + row] = v[kk];
-                    }
-                    epi_bar();
-                    int t[2], q0[2], g[2], kk[2];
-                    bool live[2];
-                    float acc[2][8];
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        const int it = et + p * EPI_THREADS;
-                        kk[p] = it >> 4;
-                        g[p] = it & 15;
-                        t[p] = c32 * 32 + kk[p];
-                        q0[p] = r0 + g[p] * 8;
-                        live[p] = t[p] < n && q0[p] < k.krv;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[p][e] = nctr == 1 ? xbm[kk[p] * RED + g[p] * 8 + e] : 0.f;
-                    }
-#pragma unroll 4
-                    for (int j = 0; j < (nctr > 1 ? nctr : 0); ++j) {
-                        const float *src = a.part + (size_t)(u0 + j) * SLOT;
-#pragma unroll
-                        for (int p = 0; p < 2; ++p)
-                            if (live[p]) add_part(src + (size_t)t[p] * TILE_M + g[p] * 8, acc[p]);
-                    }
-#pragma unroll
-                    for (int p = 0; p < 2; ++p) {
-                        if (!live[p]) continue;
-                        const float *vd = fx.tmeta[t[p]].vd;
-                        uint4 pk;
-                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
-                        if (vd && q0[p] < k.rv) {
-                            float d8[8];
-                            ld_vec8(vd + q0[p], true, 0.f, d8);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                p2[e] = __floats2bfloat162_rn(acc[p][2 * e] * d8[2 * e], acc[p][2 * e + 1] * d8[2 * e + 1]);
-                        } else {
-                            pk = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        *reinterpret_cast<uint4 *>(Ub + (size_t)t[p] * k.krv + q0[p]) = pk;
-                    }
-                    epi_bar();
-                }
-                fence_proxy_async_global();
-                __threadfence();
-                epi_bar();
-                if (et == 0) atomicAdd(sync + SY_U + U.c, 1);
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
-            if (++buf == 2) { buf = 0; bph ^= 1; }
-        }
         long long pre_to = ms;   // segments that start before pre_to have their b + v B'
         for (long long b = ms; ok && b < mend;) {
             const MLoc L = mlocate(a, b);
@@ -1058,7 +1081,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             }
             if (!ok) break;
             const int lastc = fin ? owner(fx, G, L.tb0 + L.nkb - 1) : me;
-            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true)) { ok = false; break; }
+            if (!epi_all(wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true))) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t tcol = tq + (uint32_t)(buf * 2 * BN);
             const bool my_v = k.vkb > 0 && se - L.tb0 > k.kblocks;
