@@ -16,14 +16,18 @@
 //     order) is written per layer; the owned low-rank shrink v = x A'_a runs
 //     per adapter segment;
 //   * VeRA shared shrink U = (x' A_sh) * d_a on tcgen05, cut into short
-//     K-chunks that are the first work of many CTAs, so that U is ready long
-//     before the base tiles reach their VeRA blocks;
+//     K-chunks that are the first work of many CTAs; a VeRA token is never
+//     rotated, so the chunks read x itself and start at once, and U is written
+//     right after the token operands, long before the base tiles reach their
+//     VeRA blocks;
 //   * base tiles D[128 features x BN tokens] = W^T x'^T on tcgen05 (TMA-fed,
 //     TMEM accumulators), each tile's K loop followed by the VeRA expand
 //     U B_sh as extra K blocks into a second accumulator; the 64-wide K blocks
 //     of all tiles of all layers are split over the CTAs in contiguous ranges
-//     (stream-K), and the CTA that finishes a tile last sums the other CTAs'
-//     partial tiles and applies s, b, v B' and the VeRA e in its epilogue.
+//     (stream-K).  The CTA holding a tile's first block finishes it: the CTAs
+//     sharing the tile publish their partial tiles, and the finisher adds them
+//     in CTA order to its own accumulator and applies s, b + v B' (formed one
+//     segment ahead) and the VeRA e in its epilogue.
 //
 // Waits between CTAs (token operand written, U written, v written) are
 // counters in global memory, read with acquire loads and bounded in time; the
