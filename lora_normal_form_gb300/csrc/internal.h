@@ -149,7 +149,7 @@ cudaError_t allow_max_dynamic_smem(K kernel) {
 // the epilogue warps, the VeRA shared shrink as tcgen05 K-chunks, and every
 // layer's base GEMM tiles with the VeRA expand K blocks, split over the CTAs
 // by contiguous ranges of 64-wide K blocks (stream-K), partial tiles summed
-// by the last CTA to finish each tile.
+// by the CTA holding each tile's first block.
 constexpr int STEP_MAX_CALLS = 8;
 constexpr int STEP_MAX_TOKENS = 128;
 constexpr int STEP_MAX_GRID = 190;
