@@ -629,30 +629,34 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 const StepCall &k = a.call[L.c];
                 const long long se = min(mend, L.tb0 + L.nkb);
                 int kb = L.kb;
-                if (pend_n == 0 && xs_ready(L.c, false)) {
-                    // steady state: the call's x' is written and nothing waits,
-                    // so the main blocks of the segment take a short path
-                    const CUtensorMap *mW = &k.mapW, *mQ = &k.mapXs;
-                    const int prow = L.tile * TILE_M;
-                    const long long bm = min(se, L.tb0 + (long long)k.kblocks);
-                    for (; b < bm; ++b, ++kb) {
-                        const uint32_t eb = ptx::smem_u32(&ctrl->empty[stage]);
-                        if (!ptx::mbar_try_wait(eb, phase ^ 1) && !wait_bar(eb, phase ^ 1, abort_flag, gabort)) {
-                            ok = false;
-                            break;
+                const long long bm = min(se, L.tb0 + (long long)k.kblocks);   // end of the main blocks
+                while (ok && b < se) {
+                    if (b < bm && pend_n == 0 && xs_ready(L.c, false)) {
+                        // steady state: the call's x' is written and nothing
+                        // waits, so the segment's main blocks take a short path
+                        const CUtensorMap *mW = &k.mapW, *mQ = &k.mapXs;
+                        const int prow = L.tile * TILE_M;
+                        for (; b < bm; ++b, ++kb) {
+                            const uint32_t eb = ptx::smem_u32(&ctrl->empty[stage]);
+                            if (!ptx::mbar_try_wait(eb, phase ^ 1) && !wait_bar(eb, phase ^ 1, abort_flag, gabort)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t fb = ptx::smem_u32(&ctrl->full[stage]);
+                            const uint32_t sP = s0 + (uint32_t)(stage * STAGE);
+                            ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
+                            ptx::tma_load_2d_hint(sP, mW, kb * 64, prow, fb, once);
+                            ptx::tma_load_2d_hint(sP + BOX_BYTES, mW, kb * 64, prow + BOX_ROWS, fb, once);
+                            for (int j = 0; j < BN / BOX_ROWS; ++j)
+                                ptx::tma_load_2d(sP + P_BYTES + j * BOX_BYTES, mQ, kb * 64, j * BOX_ROWS, fb);
+                            ++issued;
+                            if (++stage == S) { stage = 0; phase ^= 1; }
                         }
-                        const uint32_t fb = ptx::smem_u32(&ctrl->full[stage]);
-                        const uint32_t sP = s0 + (uint32_t)(stage * STAGE);
-                        ptx::mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
-                        ptx::tma_load_2d_hint(sP, mW, kb * 64, prow, fb, once);
-                        ptx::tma_load_2d_hint(sP + BOX_BYTES, mW, kb * 64, prow + BOX_ROWS, fb, once);
-                        for (int j = 0; j < BN / BOX_ROWS; ++j)
-                            ptx::tma_load_2d(sP + P_BYTES + j * BOX_BYTES, mQ, kb * 64, j * BOX_ROWS, fb);
-                        ++issued;
-                        if (++stage == S) { stage = 0; phase ^= 1; }
+                        continue;
                     }
-                }
-                for (; ok && b < se; ++b, ++kb) {
+                    // one block the general way (token operand not yet written,
+                    // stages pending, or a VeRA block); the short path is tried
+                    // again before the next one
                     const bool vb = kb >= k.kblocks;
                     if (vb && !((u_ok >> L.c) & 1u)) {
                         // this CTA's own pending stages may be what U waits for
@@ -663,6 +667,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     }
                     ok = vb ? issue(&k.mapBsh, L.tile * TILE_M, &k.mapU, (kb - k.kblocks) * 64, L.c, false)
                             : issue(&k.mapW, L.tile * TILE_M, &k.mapXs, kb * 64, L.c, true);
+                    ++b;
+                    ++kb;
                 }
             }
             flush(true);
