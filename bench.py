@@ -72,6 +72,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="scute", choices=["scute", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill base-GEMM leg")
     p.add_argument("--eager-steps", type=int, default=0,
                    help="only run this many untimed batched steps of the mixed workload and exit "
                         "(a fixed launch sequence for profilers); prints no JSON line")
@@ -215,6 +216,54 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+def prefill_leg(scute, dev, flush, steps=8):
+    """The prefill-shaped bf16 batch (16 requests of U{64..1024} tokens, 8772 in
+    all, one adapter each from 32 of mixed methods) through the q and gate
+    projections: the base GEMM timed by the library's event pair around its
+    launch, as TFLOP/s of 2 n d_in d_out against the bf16 tensor peak, and the
+    whole call (every kernel of the prefill path) beside it."""
+    import torch
+    _, tf_peak, peak_kind = peaks()
+    w = WL.prefill_mixed(proj=("q", "gate"))
+    ctx = scute.Context("bf16", max_tokens=w.n, max_adapters=w.n_adapters + 8, max_layers=3, device=dev.index)
+    try:
+        ctx.load_workload(w)
+        ids = torch.from_numpy(w.ids.copy()).to(dev)
+        st = torch.cuda.current_stream(dev)
+        res = {}
+        for p in ("q", "gate"):
+            L = w.layer(p)
+            x = torch.from_numpy(np.ascontiguousarray(L.get("x")).view(np.int16)).to(dev).view(torch.bfloat16)
+            out = torch.empty(w.n, L.d_out, dtype=torch.bfloat16, device=dev)
+            for _ in range(2):
+                ctx.linear(x, ids, ctx.layer_ids[p], out, "bf16", stream=st)
+            torch.cuda.synchronize()
+            ctx.timing(True)
+            ctx.timing_reset()
+            call_ms = []
+            for _ in range(steps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                ctx.linear(x, ids, ctx.layer_ids[p], out, "bf16", stream=st)
+                e1.record(st)
+                e1.synchronize()
+                call_ms.append(e0.elapsed_time(e1))
+            gemm_ms = ctx.timing_read()
+            ctx.timing(False)
+            g = float(np.median(np.array(gemm_ms[-steps:], dtype=np.float64)))
+            tflops = 2.0 * w.n * L.d_in * L.d_out / (g * 1e-3) / 1e12
+            res[p] = {"shape": f"{L.d_in}->{L.d_out}", "base_gemm_ms": g, "achieved": tflops,
+                      "frac": tflops / tf_peak, "call_ms": float(np.median(call_ms))}
+        if ctx.sync_status() != 0:
+            raise RuntimeError("device status error in the prefill leg")
+        return {"workload": f"prefill_mixed: {w.n} tokens, q and gate projections", "bound": "tensor",
+                "unit": "TFLOP/s", "peak": tf_peak, "peak_kind": peak_kind, "per_projection": res}
+    finally:
+        ctx.close()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -412,6 +461,11 @@ def main():
         "launches_per_step": int(launches_per_step),
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_prefill:
+        try:
+            line["prefill"] = prefill_leg(scute, dev, flush)
+        except Exception as exc:   # the headline line is printed whatever this leg does
+            line["prefill"] = {"error": str(exc)[:300]}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
