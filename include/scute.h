@@ -118,7 +118,9 @@ scute_status scute_set_shared(scute_ctx *ctx, int layer, int rank, const void *A
  *   LORA  A [d_in, rank], B [rank, d_out], c (= alpha / rank), rank
  *   DORA  A, B, c, rank, magnitude [d_out] (learned column length m)
  *   IA3   l [d_out]
- *   VERA  d [shared rank], e [d_out]     (the layer must have a shared pair)
+ *   VERA  d [shared rank], e [d_out], c  (the layer must have a shared pair;
+ *         c scales the shared term and is applied as given, like every other
+ *         term's c: 1 for plain VeRA, 0 switches the term off)
  *   OFT   R [d_in/32, 32, 32]
  *   NF    any of s [d_out], b [d_out], R, and one owned term A, B, rank, c with
  *         optional d [rank] and e [d_out]
@@ -267,7 +269,10 @@ scute_status scute_debug_index(scute_ctx *ctx, const int32_t *adapter_ids, int64
  * Scratch: a file-scope device array of SCUTE_NOALLOC_SCRATCH_BYTES (the method
  * table and a status word), located once per device with cudaGetSymbolAddress
  * on the first call made while that device is current.  That first call may
- * load the library's module, so make it before any stream capture.  Nothing
+ * load the library's module, so make it before any stream capture.  The
+ * address is kept for the life of the process: do not use this call on a
+ * device after cudaDeviceReset (or any teardown of its primary context) in
+ * the same process.  Nothing
  * is allocated: no cudaMalloc, cudaFree or allocating library routine.
  * Overlapping calls on one device (other streams, other host threads) share
  * the array and race; order them on the device.
@@ -357,6 +362,15 @@ scute_status scute_timing_read(scute_ctx *ctx, float *ms_out, int max, int *n_ou
  * the hook applies to that one launch only.  Nothing traps or faults. */
 #define SCUTE_INJECT_STALL 1
 scute_status scute_debug_inject(scute_ctx *ctx, int what);
+
+/* Test hook for the out-of-memory path (no counterpart in the article).  The
+ * k-th device allocation the library makes after this call (counted over
+ * every context of the process) fails as if the device were out of memory:
+ * nothing is allocated for it and the call that needed it returns
+ * SCUTE_ERR_OOM, having freed what it had allocated itself and leaving the
+ * context as it was.  k <= 0 switches the hook off.  Host-side only: no
+ * device work is involved. */
+void scute_debug_fail_alloc(int k);
 
 #ifdef __cplusplus
 }

@@ -112,6 +112,7 @@ _SIGS = {
     "scute_timing_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_timing_reset": (ctypes.c_int, [ctypes.c_void_p]),
     "scute_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "scute_debug_fail_alloc": (None, [ctypes.c_int]),
     "scute_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]),
 }
@@ -150,7 +151,14 @@ def ptr(x) -> Optional[int]:
 
 
 def _stream_handle(stream) -> Optional[int]:
+    """The cudaStream_t to pass: an int as given, a torch stream's handle, or,
+    for None, torch's current stream on the current device (so that calls
+    made under ``torch.cuda.stream(s)`` are ordered with that stream's work)."""
     if stream is None:
+        import sys
+        torch = sys.modules.get("torch")
+        if torch is not None and torch.cuda.is_available() and torch.cuda.is_initialized():
+            return torch.cuda.current_stream().cuda_stream
         return None
     if isinstance(stream, int):
         return stream
@@ -298,6 +306,12 @@ INJECT_STALL = 1
 
 def scute_debug_inject(ctx, what: int) -> None:
     _check(ctx, load().scute_debug_inject(ctx, what))
+
+
+def scute_debug_fail_alloc(k: int) -> None:
+    """Make the k-th device allocation of the library from now fail as out of
+    memory (test hook; k <= 0 switches it off)."""
+    load().scute_debug_fail_alloc(int(k))
 
 
 def scute_timing_read(ctx, max_slots: int = TIMING_SLOTS) -> list:

@@ -1,6 +1,7 @@
 // Host runtime of libscute.so: contexts, layers, adapter registration with the
 // fold rule, the per-call launch plan of the adapted linear layer, the byte
 // model and the timing counters.  See include/scute.h for the contract.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -49,6 +50,25 @@ struct DeviceGuard {
     }
 };
 
+// Test hook scute_debug_fail_alloc: while positive, counts the library's
+// device allocations down; the allocation that brings it from 1 to 0 fails as
+// if the device were out of memory (nothing is allocated for it).
+std::atomic<int> g_fail_alloc{0};
+
+cudaError_t dev_malloc(void **p, size_t bytes) {
+    int k = g_fail_alloc.load();
+    while (k > 0) {
+        if (g_fail_alloc.compare_exchange_weak(k, k - 1)) {
+            if (k == 1) {
+                *p = nullptr;
+                return cudaErrorMemoryAllocation;
+            }
+            break;
+        }
+    }
+    return cudaMalloc(p, bytes);
+}
+
 bool encode_map(scute_ctx *c, CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {inner * (uint64_t)c->esz};
@@ -66,8 +86,12 @@ scute_status grow(scute_ctx *c, void **buf, size_t *cols, size_t need_cols, size
     if (need_cols <= *cols) return SCUTE_OK;
     void *p = nullptr;
     CU_TRY(c, cudaDeviceSynchronize());
-    CU_TRY(c, cudaMalloc(&p, need_cols * elem_bytes * rows));
-    CU_TRY(c, cudaMemset(p, 0, need_cols * elem_bytes * rows));
+    CU_TRY(c, dev_malloc(&p, need_cols * elem_bytes * rows));
+    const cudaError_t e = cudaMemset(p, 0, need_cols * elem_bytes * rows);
+    if (e != cudaSuccess) {
+        cudaFree(p);
+        CU_TRY(c, e);
+    }
     if (*buf) cudaFree(*buf);
     *buf = p;
     *cols = need_cols;
@@ -91,7 +115,7 @@ scute_status ensure_tmp(scute_ctx *c, size_t bytes) {
     if (c->tmp) cudaFree(c->tmp);
     c->tmp = nullptr;
     c->tmp_bytes = 0;
-    CU_TRY(c, cudaMalloc(&c->tmp, bytes));
+    CU_TRY(c, dev_malloc(&c->tmp, bytes));
     c->tmp_bytes = bytes;
     return SCUTE_OK;
 }
@@ -146,24 +170,24 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
     }
     c->encode = reinterpret_cast<PFN_encodeTiled>(fn);
     const size_t nslots = (size_t)max_layers * max_adapters;
-    bool ok = cudaMalloc(&c->d_slots, nslots * sizeof(Slot)) == cudaSuccess &&
+    bool ok = dev_malloc((void **)&c->d_slots, nslots * sizeof(Slot)) == cudaSuccess &&
               cudaMemset(c->d_slots, 0, nslots * sizeof(Slot)) == cudaSuccess &&
-              cudaMalloc(&c->d_method, max_adapters) == cudaSuccess &&
+              dev_malloc((void **)&c->d_method, max_adapters) == cudaSuccess &&
               cudaMemset(c->d_method, 0xFF, max_adapters) == cudaSuccess &&
-              cudaMalloc(&c->d_perm, sizeof(int) * max_tokens) == cudaSuccess &&
-              cudaMalloc(&c->d_aid, sizeof(int) * max_tokens) == cudaSuccess &&
-              cudaMalloc(&c->d_seg_start, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
-              cudaMalloc(&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
-              cudaMalloc(&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
+              dev_malloc((void **)&c->d_perm, sizeof(int) * max_tokens) == cudaSuccess &&
+              dev_malloc((void **)&c->d_aid, sizeof(int) * max_tokens) == cudaSuccess &&
+              dev_malloc((void **)&c->d_seg_start, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
+              dev_malloc((void **)&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
+              dev_malloc((void **)&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
               cudaMemset(c->d_meta, 0, sizeof(IndexMeta)) == cudaSuccess &&
-              cudaMalloc(&c->d_status, sizeof(int)) == cudaSuccess &&
+              dev_malloc((void **)&c->d_status, sizeof(int)) == cudaSuccess &&
               cudaMemset(c->d_status, 0, sizeof(int)) == cudaSuccess &&
-              cudaMalloc(&c->d_err, sizeof(int)) == cudaSuccess &&
-              cudaMalloc(&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
-              cudaMalloc(&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess &&
-              cudaMalloc(&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess &&
-              cudaMalloc(&c->step_v, sizeof(float) * STEP_MAX_CALLS * STEP_MAX_TOKENS * MAX_RANK) == cudaSuccess &&
-              cudaMalloc(&c->step_sync, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
+              dev_malloc((void **)&c->d_err, sizeof(int)) == cudaSuccess &&
+              dev_malloc((void **)&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
+              dev_malloc((void **)&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess &&
+              dev_malloc((void **)&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess &&
+              dev_malloc((void **)&c->step_v, sizeof(float) * STEP_MAX_CALLS * STEP_MAX_TOKENS * MAX_RANK) == cudaSuccess &&
+              dev_malloc((void **)&c->step_sync, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
               cudaMemset(c->step_sync, 0, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
               cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) ==
                   cudaSuccess;
@@ -216,10 +240,16 @@ scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const
     L.kdim = f32 ? 3 * d_in : d_in;
     scute_status st = ensure_tmp(c, (size_t)d_in * d_out * c->esz);
     if (st) return st;
-    CU_TRY(c, cudaMalloc(&L.Wt, (size_t)d_out * L.kdim * c->esz));
-    CU_TRY(c, cudaMemcpy(c->tmp, W, (size_t)d_in * d_out * c->esz, cudaMemcpyDefault));
-    CU_TRY(c, launch_transpose_w(f32, c->tmp, d_in, d_out, L.Wt, L.kdim, f32 ? 1 : 0, 0));
-    CU_TRY(c, cudaDeviceSynchronize());
+    CU_TRY(c, dev_malloc(&L.Wt, (size_t)d_out * L.kdim * c->esz));
+    {
+        cudaError_t e = cudaMemcpy(c->tmp, W, (size_t)d_in * d_out * c->esz, cudaMemcpyDefault);
+        if (e == cudaSuccess) e = launch_transpose_w(f32, c->tmp, d_in, d_out, L.Wt, L.kdim, f32 ? 1 : 0, 0);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            cudaFree(L.Wt);
+            CU_TRY(c, e);
+        }
+    }
     if (!encode_map(c, &L.mapW, L.Wt, (uint64_t)L.kdim, (uint64_t)d_out)) {
         cudaFree(L.Wt);
         return fail(c, SCUTE_ERR_CUDA, "tensor map for W failed");
@@ -246,8 +276,11 @@ scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const
         c->step_part = reinterpret_cast<float *>(pp);
     }
     if (st) {
+        // the layer is not added; buffers that did grow have moved, so the
+        // other layers' tensor maps are refreshed before returning
         cudaFree(c->layers[layer].Wt);
         c->layers[layer] = LayerRec();
+        remap_workspace(c);
         return st;
     }
     (void)old_xs;
@@ -270,28 +303,41 @@ scute_status scute_set_shared(scute_ctx *c, int layer, int rank, const void *A_s
     scute_status st = ensure_tmp(c, big * c->esz);
     if (st) return st;
     void *Ash = nullptr, *Bsh = nullptr;
-    CU_TRY(c, cudaMalloc(&Ash, (size_t)rank * L.kdim * c->esz));
-    CU_TRY(c, cudaMalloc(&Bsh, (size_t)L.d_out * krv * c->esz));
-    CU_TRY(c, cudaMemcpy(c->tmp, A_sh, (size_t)L.d_in * rank * c->esz, cudaMemcpyDefault));
-    CU_TRY(c, launch_transpose_w(f32, c->tmp, L.d_in, rank, Ash, L.kdim, f32 ? 1 : 0, 0));
-    CU_TRY(c, cudaDeviceSynchronize());
-    CU_TRY(c, cudaMemcpy(c->tmp, B_sh, (size_t)rank * L.d_out * c->esz, cudaMemcpyDefault));
-    CU_TRY(c, launch_transpose_w(f32, c->tmp, rank, L.d_out, Bsh, krv, f32 ? 1 : 0, 0));
-    CU_TRY(c, cudaDeviceSynchronize());
+    {
+        cudaError_t e = dev_malloc(&Ash, (size_t)rank * L.kdim * c->esz);
+        if (e == cudaSuccess) e = dev_malloc(&Bsh, (size_t)L.d_out * krv * c->esz);
+        if (e == cudaSuccess) e = cudaMemcpy(c->tmp, A_sh, (size_t)L.d_in * rank * c->esz, cudaMemcpyDefault);
+        if (e == cudaSuccess) e = launch_transpose_w(f32, c->tmp, L.d_in, rank, Ash, L.kdim, f32 ? 1 : 0, 0);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaMemcpy(c->tmp, B_sh, (size_t)rank * L.d_out * c->esz, cudaMemcpyDefault);
+        if (e == cudaSuccess) e = launch_transpose_w(f32, c->tmp, rank, L.d_out, Bsh, krv, f32 ? 1 : 0, 0);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            if (Ash) cudaFree(Ash);
+            if (Bsh) cudaFree(Bsh);
+            CU_TRY(c, e);
+        }
+    }
     if (!encode_map(c, &L.mapAsh, Ash, (uint64_t)L.kdim, (uint64_t)rank) ||
         !encode_map(c, &L.mapBsh, Bsh, (uint64_t)krv, (uint64_t)L.d_out)) {
         cudaFree(Ash);
         cudaFree(Bsh);
         return fail(c, SCUTE_ERR_CUDA, "tensor map for the shared pair failed");
     }
+    // the VeRA intermediates must hold the new rank before the layer uses it
+    st = grow(c, &c->U, &c->u_cols, (size_t)krv, c->esz, c->max_tokens);
+    if (!st && !f32) st = grow(c, &c->step_U, &c->step_u_cols, (size_t)krv, c->esz,
+                               (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS);
+    if (st) {
+        cudaFree(Ash);
+        cudaFree(Bsh);
+        remap_workspace(c);   // U may have moved
+        return st;
+    }
     L.Ash = Ash;
     L.Bsh = Bsh;
     L.rv = rank;
     L.krv = krv;
-    st = grow(c, &c->U, &c->u_cols, (size_t)krv, c->esz, c->max_tokens);
-    if (!st && !f32) st = grow(c, &c->step_U, &c->step_u_cols, (size_t)krv, c->esz,
-                               (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS);
-    if (st) return st;
     return remap_workspace(c);
 }
 
@@ -371,7 +417,7 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
     scute_status st = ensure_tmp(c, tmp_need ? tmp_need : 256);
     if (st) return st;
     void *storage = nullptr;
-    CU_TRY(c, cudaMalloc(&storage, total ? total : 256));
+    CU_TRY(c, dev_malloc(&storage, total ? total : 256));
     uint8_t *cur = reinterpret_cast<uint8_t *>(storage);
     auto take = [&](size_t bytes) {
         void *p = cur;
@@ -383,7 +429,9 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
         cudaError_t _e = (expr);                                                       \
         if (_e != cudaSuccess) {                                                       \
             cudaFree(storage);                                                         \
-            return fail(c, SCUTE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e));   \
+            (void)cudaGetLastError();                                                  \
+            return fail(c, _e == cudaErrorMemoryAllocation ? SCUTE_ERR_OOM : SCUTE_ERR_CUDA, \
+                        "%s: %s", #expr, cudaGetErrorString(_e));                      \
         }                                                                              \
     } while (0)
     REG_TRY(cudaMemset(c->d_err, 0, sizeof(int)));
@@ -461,7 +509,8 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
             float *td = reinterpret_cast<float *>(tmp);
             REG_TRY(cudaMemcpy(td, x.d, 4 * (size_t)L.rv, cudaMemcpyDefault));
             // the shared term's scalar c is the adapter's own: merged into its d
-            REG_TRY(launch_scale_vec(td, x.c == 0.f ? 1.f : x.c, dp, L.rv, 0));
+            // (applied as given, like every other term's c)
+            REG_TRY(launch_scale_vec(td, x.c, dp, L.rv, 0));
             if (x.e) {
                 REG_TRY(cudaMemcpy(ep, x.e, 4 * (size_t)L.d_out, cudaMemcpyDefault));
                 s.ve = ep;
@@ -980,6 +1029,8 @@ scute_status scute_timing_reset(scute_ctx *c) {
     c->t_used = 0;
     return SCUTE_OK;
 }
+
+void scute_debug_fail_alloc(int k) { g_fail_alloc.store(k > 0 ? k : 0); }
 
 scute_status scute_debug_inject(scute_ctx *c, int what) {
     if (!c) return SCUTE_ERR_ARG;

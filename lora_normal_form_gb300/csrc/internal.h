@@ -4,6 +4,7 @@
 
 #include <cuda.h>  // CUtensorMap type only; the driver entry point is fetched at run time
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -127,17 +128,25 @@ inline int lowrank_ks(int d_in, int *kchunk_out) {
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum
-// less its static shared memory (asked once per kernel).
+// less its static shared memory.  A function attribute belongs to one device
+// context, so the raise is made once per (kernel, device): `done` holds one bit
+// per device id below 64 (devices beyond that ask on every launch).  Two host
+// threads racing on the first launch both set the same value, which is
+// harmless.
 template <typename K>
-cudaError_t allow_max_dynamic_smem(K kernel) {
+cudaError_t allow_max_dynamic_smem(K kernel, std::atomic<unsigned long long> &done) {
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
     return e;
 }
 

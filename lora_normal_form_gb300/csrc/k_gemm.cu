@@ -16,8 +16,10 @@
 // Shape of one work tile: D[128 x BN] = P[128 rows, K] * Q[BN rows, K]^T with
 // both operands K-major.  For small token counts (decode) the features sit on
 // the 128-row P side and the tokens on the BN side (P = W^T, Q = x'), and the
-// K dimension is split over a thread-block cluster whose partial tiles are
-// reduced through distributed shared memory.  For large token counts
+// K dimension is split over a thread-block cluster: each CTA of the cluster
+// writes its partial tile to an L2-resident workspace in global memory, and
+// after a cluster barrier the CTAs read back each other's slices and sum
+// them.  For large token counts
 // (prefill) tokens sit on P and features on Q, and a persistent grid walks the
 // tiles with a double-buffered TMEM accumulator.
 //
@@ -714,12 +716,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
 
 template <int BN, bool TF32>
 cudaError_t launch_one(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl) {
-    static bool attr_set = false;
+    static std::atomic<unsigned long long> attr_done{0};
     auto kern = gemm_tc_kernel<BN, TF32>;
-    if (!attr_set) {
-        cudaError_t e = allow_max_dynamic_smem(kern);
+    {
+        const cudaError_t e = allow_max_dynamic_smem(kern, attr_done);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);

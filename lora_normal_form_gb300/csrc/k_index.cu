@@ -180,11 +180,10 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
                          int *status, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = allow_max_dynamic_smem(index_kernel);
+    static std::atomic<unsigned long long> attr_done{0};
+    {
+        const cudaError_t e = allow_max_dynamic_smem(index_kernel, attr_done);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     const int threads = n <= 2048 ? 256 : 1024;
     const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * 256 * sizeof(int);

@@ -1286,11 +1286,10 @@ size_t step_smem_bytes(int bn, int stages, int rmax) {
 }
 
 cudaError_t launch_step(const StepArgs &a, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = allow_max_dynamic_smem(step_kernel);
+    static std::atomic<unsigned long long> attr_done{0};
+    {
+        const cudaError_t e = allow_max_dynamic_smem(step_kernel, attr_done);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.grid, 1, 1);

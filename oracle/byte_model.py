@@ -4,9 +4,9 @@ Test infrastructure only (see ``oracle/__init__``).
 
 The article ("Where is the cheapest place to compute the remaining slots?")
 measures adapter work in bytes moved and predicts added time as extra bytes /
-bandwidth + extra launches x launch cost.  The definition used for this build
-(written out in DESIGN.md, "Byte model") counts, per kernel launch of the
-call, every operand read once and every result written once, and for the call
+bandwidth + extra launches x launch cost.  The definition restated here
+counts, per kernel launch of the call, every operand read once and every
+result written once, and for the call
 its algorithmic bytes: W once, each distinct adapter's live tensors once, the
 shared VeRA pair once when a VeRA token is present, x read, out written, ids
 read.  This module computes those integers with plain Python loops.

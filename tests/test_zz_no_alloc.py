@@ -1,9 +1,16 @@
-"""Context-free token indexing that allocates nothing (scute_index_tokens_noalloc),
-against the context's own indexing call (scute_debug_index) on the same ids.
+"""Context-free token indexing that allocates nothing
+(scute_index_tokens_noalloc), graded directly against the oracle's indexing
+(a stable sort by (method, adapter id)) bit for bit, and against the context's
+own indexing call (scute_debug_index) on the same ids.
 
-Both run the same sorting kernel, so the comparison is bit for bit.  The file
-is named to be collected last, so that it also runs after every other test has
-used the device; it needs nothing from them and passes alone too."""
+Who needs the entry point: callers that cannot allocate device memory, such as
+a scheduler that shares the GPU with an engine whose memory pool already holds
+most of HBM, or latency-critical code where cudaMalloc may synchronise.  The
+tests check the property it is named for too: after a first call, further
+calls change neither the device's free memory nor torch's allocations.
+
+The file is named to be collected last, so that it also runs after every other
+test has used the device; it needs nothing from them and passes alone too."""
 import numpy as np
 import pytest
 
@@ -55,34 +62,88 @@ def setup(gpu_lib):
 def _outputs(n):
     i32 = dict(dtype=torch.int32, device="cuda")
     return (torch.full((n,), -7, **i32), torch.full((n,), -7, **i32), torch.full((n + 1,), -7, **i32),
-            torch.full((n,), -7, **i32), torch.full((22,), -7, **i32))
+            torch.full((max(n, 1),), -7, **i32), torch.full((22,), -7, **i32))
+
+
+def _assert_matches_oracle(got, ids, methods):
+    """The entry point's arrays against the oracle's stable sort, bit for bit."""
+    n = ids.size
+    ref = IX.index_tokens(ids, methods, A)
+    perm, aid, seg_start, seg_aid, counts = (t.cpu().numpy() for t in got)
+    n_seg = int(counts[0])
+    assert n_seg == len(ref.seg_aid)
+    np.testing.assert_array_equal(perm[:n], ref.perm)
+    np.testing.assert_array_equal(aid[:n], ref.aid_sorted)
+    np.testing.assert_array_equal(seg_start[:n_seg + 1], ref.seg_start)
+    np.testing.assert_array_equal(seg_aid[:n_seg], ref.seg_aid)
+    np.testing.assert_array_equal(counts[1:8], ref.count)
+    np.testing.assert_array_equal(counts[8:15], ref.offset)
+    return ref
 
 
 @pytest.mark.parametrize("sizes", [(300, 2049), (1, 64)])
-def test_noalloc_matches_context_indexing_twice(setup, sizes):
+def test_noalloc_matches_oracle_and_context_twice(setup, sizes):
+    """Two calls in a row: the first with unregistered ids (flag set), the
+    second without, so a status word that was not cleared between calls would
+    show as a stale flag.  Each is graded against the oracle and against the
+    context's indexing call."""
     scute, ctx, methods, table = setup
     for call, n in enumerate(sizes):
         g = np.random.default_rng(1000 + n)
-        # first call: unregistered ids included (flag set); second: none, so a
-        # status word that was not cleared would show up as a stale flag
         ids = g.integers(-1, A if call == 0 else A - 2, n).astype(np.int32)
         if call == 0:
             ids[n // 2] = A - 1
         ids_t = torch.from_numpy(ids).cuda()
-        ref = _outputs(n)
-        ctx.debug_index(ids_t, n, *ref)
         got = _outputs(n)
         flags = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
         scute.scute_index_tokens_noalloc(table, ids_t, n, *got, flags=flags)
         torch.cuda.synchronize()
-        n_seg = int(ref[4][0].item())
-        assert int(got[4][0].item()) == n_seg
-        for a, b, k in zip(got, ref, (n, n, n_seg + 1, n_seg, 22)):
+        ref = _assert_matches_oracle(got, ids, methods)
+        assert (int(flags.item()) != 0) == bool(ref.bad)
+        assert bool(ref.bad) == (call == 0)
+        # and the context's own indexing call agrees with it
+        ctxo = _outputs(n)
+        ctx.debug_index(ids_t, n, *ctxo)
+        torch.cuda.synchronize()
+        n_seg = int(ctxo[4][0].item())
+        for a, b, k in zip(got, ctxo, (n, n, n_seg + 1, n_seg, 22)):
             np.testing.assert_array_equal(a.cpu().numpy()[:k], b.cpu().numpy()[:k])
-        bad = IX.index_tokens(ids, methods, A).bad
-        assert (int(flags.item()) != 0) == bool(bad)
-        assert ctx.sync_status() == (5 if bad else 0)
-        assert bad == (call == 0)
+        assert ctx.sync_status() == (5 if ref.bad else 0)
+
+
+def test_noalloc_allocates_nothing_on_a_side_stream(setup):
+    """After a first call, further calls (on a non-default stream, of
+    several sizes, n = 0 included) leave the device's free memory and torch's
+    allocations unchanged; results are still the oracle's."""
+    scute, _, methods, table = setup
+    g = np.random.default_rng(7)
+    cases = [g.integers(-1, A - 2, n).astype(np.int32) for n in (513, 0, 4096, 1)]
+    bufs = [(torch.from_numpy(ids).cuda(), _outputs(ids.size)) for ids in cases]
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    # first call: may load the library's module and look up the scratch array
+    with torch.cuda.stream(s):
+        scute.scute_index_tokens_noalloc(table, bufs[0][0], cases[0].size, *bufs[0][1], flags=flags,
+                                         stream=s)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for rep in range(2):
+        for ids, (ids_t, out) in zip(cases, bufs):
+            with torch.cuda.stream(s):
+                scute.scute_index_tokens_noalloc(table, ids_t, ids.size, *out, flags=flags, stream=s)
+            s.synchronize()
+            assert int(flags.item()) == 0
+            if ids.size == 0:
+                c = out[4].cpu().numpy()
+                assert int(out[2][0].item()) == 0 and c[0] == 0 and (c[1:] == 0).all()
+            else:
+                _assert_matches_oracle(out, ids, methods)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
 
 
 def test_noalloc_rejects_sizes_beyond_its_limits(setup):

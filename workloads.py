@@ -258,10 +258,15 @@ def uniform_ids(seed, n, n_adapters) -> np.ndarray:
     return _rng(seed, "ids").integers(0, n_adapters, n).astype(np.int32)
 
 
-def request_ids(seed, n_req, lo, hi, n_adapters) -> Tuple[np.ndarray, np.ndarray]:
-    """Prefill batch: request lengths U{lo..hi}, one adapter per request."""
+def request_ids(seed, n_req, lo, hi, n_adapters, req_adapters=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Prefill batch: request lengths U{lo..hi}, one adapter per request (drawn
+    uniformly from the pool, or the given ``req_adapters``)."""
     lens = np.random.default_rng(seed).integers(lo, hi + 1, n_req)
-    ads = _rng(seed, "req_adapters").integers(0, n_adapters, n_req)
+    if req_adapters is None:
+        ads = _rng(seed, "req_adapters").integers(0, n_adapters, n_req)
+    else:
+        ads = np.asarray(req_adapters, dtype=np.int64)
+        assert ads.shape == (n_req,) and ads.min() >= -1 and ads.max() < n_adapters
     return np.repeat(ads, lens).astype(np.int32), lens
 
 
@@ -312,10 +317,12 @@ def decode_mixed(seed: int = 0, n: int = 64, n_adapters: int = 32, rank: int = 1
 def prefill_mixed(seed: int = 0, n_req: int = 16, lo: int = 64, hi: int = 1024,
                   n_adapters: int = 32, rank: int = 16, rv: int = 256,
                   proj=("q", "k", "v", "gate", "up", "down"), shapes=None,
-                  dtype: str = "bf16") -> Workload:
+                  dtype: str = "bf16", req_adapters=None) -> Workload:
     """Same shapes, bf16 prefill: n_req requests with lengths U{lo..hi}, each
-    request one adapter drawn uniformly from the pool."""
-    ids, lens = request_ids(seed, n_req, lo, hi, n_adapters)
+    request one adapter drawn uniformly from the pool (or the adapters listed
+    in ``req_adapters``, one per request: a parity case that puts every method
+    in one prefill batch; the seed-0 draw happens to pick no OFT adapter)."""
+    ids, lens = request_ids(seed, n_req, lo, hi, n_adapters, req_adapters)
     w = decode_mixed(seed, n=int(ids.size), n_adapters=n_adapters, rank=rank, rv=rv,
                      proj=proj, shapes=shapes, ids=ids, dtype=dtype, name="prefill_mixed")
     w.recipe = (f"{n_req} requests, lengths U{{{lo}..{hi}}} (sum {ids.size}), one adapter "
