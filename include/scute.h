@@ -289,19 +289,24 @@ scute_status scute_index_tokens_noalloc(const int8_t *method_of_adapter, int32_t
                                         int32_t *counts, int32_t *flags, void *stream);
 
 /* ---------------------------------------------------------------- byte model
- * Zero-parameter byte model (article, section "Where is the cheapest place to
- * compute the remaining slots?": added time = extra bytes / memory bandwidth +
- * extra launches x launch cost; bytes are what adapter work is measured in).
+ * Zero-parameter byte and time model (article, section "Where is the cheapest
+ * place to compute the remaining slots?": added time = extra bytes / memory
+ * bandwidth + extra launches x launch cost; bytes are what adapter work is
+ * measured in).
  *
- * For one scute_linear call it lists every kernel launch with the bytes it
- * must move to and from device memory (each operand read once, each result
- * written once: a lower bound that the measured DRAM bytes are compared
- * against) and its floating-point operations, plus the call's algorithmic
- * bytes: W once, each distinct adapter's live (post-fold) tensors once, the
- * shared VeRA pair once when a VeRA token is present, x read, out written and
- * the ids read.  Pure host arithmetic: no device work, no context needed for
- * scute_byte_model. */
-#define SCUTE_BM_MAX_KERNELS 8
+ * For one call it lists every kernel launch the library makes for it, with the
+ * bytes that launch must move to and from device memory (each operand read
+ * once, each result written once; intermediates a launch keeps to itself are
+ * not counted: a lower bound that measured DRAM bytes are compared against)
+ * and its floating-point operations, plus the call's algorithmic bytes: W once,
+ * each distinct adapter's live (post-fold) tensors once, the shared VeRA pair
+ * once when a VeRA token is present, x read, out written and the ids read.
+ * Launch plans: a bf16 batch of at most 128 tokens is ONE launch ("step") over
+ * every layer of the call; otherwise each layer takes the per-kernel plan
+ * ("index", "rotate", "base_gemm", "lr_shrink", "lr_expand", "vera_shrink",
+ * "vera_expand").  Pure host arithmetic: no device work, no context needed for
+ * scute_byte_model and scute_byte_model_batch. */
+#define SCUTE_BM_MAX_KERNELS 64
 typedef struct {
     int n_kernels;                          /* launches of the call            */
     char name[SCUTE_BM_MAX_KERNELS][24];    /* kernel names                    */
@@ -326,33 +331,71 @@ typedef struct {
     scute_dtype out_dtype;
     int d_in, d_out;
     int shared_rank;          /* 0 = no shared VeRA pair                       */
-    int lowrank_launched;     /* the call launches the owned-term kernels      */
-    int vera_launched;        /* the call launches the VeRA kernels            */
+    int lowrank_launched;     /* the per-kernel plan launches the owned-term kernels */
+    int vera_launched;        /* the per-kernel plan launches the VeRA kernels */
     int max_adapters;
     const scute_bm_adapter *adapters;  /* [max_adapters]                       */
 } scute_bm_layer;
 
+/* One call of one layer (scute_linear). */
 scute_status scute_byte_model(const scute_bm_layer *layer, const int32_t *ids_host, int64_t n,
                               scute_byte_report *rep);
+
+/* One batched call (scute_linear_batch) over n_layers (1..SCUTE_MAX_CALLS)
+ * layers that read the same ids; all in one dtype.  SCUTE_ERR_UNSUPPORTED when
+ * the per-kernel plan needs more than SCUTE_BM_MAX_KERNELS launches. */
+scute_status scute_byte_model_batch(const scute_bm_layer *layers, int n_layers, const int32_t *ids_host,
+                                    int64_t n, scute_byte_report *rep);
 
 /* The same for layer `layer` of a context, from its registered adapters. */
 scute_status scute_predict_bytes(const scute_ctx *ctx, const int32_t *ids_host, int64_t n,
                                  int layer, scute_dtype out_dtype, scute_byte_report *rep);
+
+/* The same for a batched call of a context (only calls[i].layer is read). */
+scute_status scute_predict_batch(const scute_ctx *ctx, const scute_call *calls, int n_calls,
+                                 const int32_t *ids_host, int64_t n, scute_dtype out_dtype,
+                                 scute_byte_report *rep);
+
+/* Predicted time of a launch list, in microseconds:
+ *     sum over launches of max(bytes / hbm_gbs, flops / tensor_tflops)
+ *     + launches x launch_us.
+ * With tensor_tflops <= 0 the flops term is dropped and this is the article's
+ * model as it stands (bytes / bandwidth + launches x launch cost); the flops
+ * term extends it to launches bound by the tensor cores (prefill GEMMs).  The
+ * three constants are measured on the device, never fitted. */
+scute_status scute_predict_time(const scute_byte_report *rep, double hbm_gbs, double tensor_tflops,
+                                double launch_us, double *us_out);
 
 /* ---------------------------------------------------------------- counters
  * Device kernels enqueued by this context since creation. */
 int64_t scute_launch_count(const scute_ctx *ctx);
 
 /* Kernel timing with CUDA events on the launching stream.  While enabled,
- * every scute_linear records an event pair around its base GEMM launch into a
- * ring of `SCUTE_TIMING_SLOTS` slots (slot = call count modulo the ring; event
- * records made during stream capture become graph nodes and are re-recorded on
- * every replay).  scute_timing_read synchronises the device and writes the
- * elapsed milliseconds of the first `max` used slots. */
+ * every launch of the hot path (the decode step; or, on the per-kernel plan,
+ * the indexing, rotation, base GEMM, low-rank shrink + expand pair and the two
+ * VeRA GEMMs) is bracketed by an event pair, stored in a ring of
+ * `SCUTE_TIMING_SLOTS` slots in launch order and tagged with its kind
+ * (SCUTE_KIND_*).  Event records made during stream capture become graph
+ * nodes and are re-recorded on every replay.  Timing puts an event record
+ * between launches that would otherwise overlap their start and end
+ * (programmatic dependent launch), so a timed call can be slightly slower.
+ * scute_timing_read synchronises the device and writes the elapsed
+ * milliseconds of the first `max` used slots; scute_timing_kinds writes their
+ * kinds. */
 #define SCUTE_TIMING_SLOTS 256
+enum {
+    SCUTE_KIND_STEP = 0,         /* the batched decode step (one launch)       */
+    SCUTE_KIND_INDEX = 1,        /* token indexing                             */
+    SCUTE_KIND_ROTATE = 2,       /* OFT rotation / gather of the token operand */
+    SCUTE_KIND_BASE_GEMM = 3,    /* base GEMM with the s / b epilogue          */
+    SCUTE_KIND_LOWRANK = 4,      /* owned low-rank shrink and expand (2 launches) */
+    SCUTE_KIND_VERA_SHRINK = 5,  /* VeRA shared shrink GEMM                    */
+    SCUTE_KIND_VERA_EXPAND = 6   /* VeRA shared expand GEMM                    */
+};
 scute_status scute_timing_enable(scute_ctx *ctx, int enable);
 scute_status scute_timing_reset(scute_ctx *ctx);
 scute_status scute_timing_read(scute_ctx *ctx, float *ms_out, int max, int *n_out);
+scute_status scute_timing_kinds(const scute_ctx *ctx, int *kinds_out, int max, int *n_out);
 
 /* Test hook for the failure path (no counterpart in the article).  With
  * what = SCUTE_INJECT_STALL, the context's next decode launch (bf16, n <= 128)

@@ -24,7 +24,7 @@ STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_DTYPE", 4: "ERR_OOM", 5
           6: "ERR_CUDA", 7: "ERR_TIMEOUT", 8: "ERR_UNSUPPORTED", 9: "ERR_NO_DEVICE"}
 MAX_TOKENS = 16384
 TIMING_SLOTS = 256
-BM_MAX_KERNELS = 8
+BM_MAX_KERNELS = 64
 
 
 class ScuteError(RuntimeError):
@@ -108,6 +108,12 @@ _SIGS = {
                                         ctypes.POINTER(ByteReport)]),
     "scute_predict_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.POINTER(ByteReport)]),
+    "scute_byte_model_batch": (ctypes.c_int, [ctypes.POINTER(BmLayer), ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_int64, ctypes.POINTER(ByteReport)]),
+    "scute_predict_batch": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Call), ctypes.c_int, ctypes.c_void_p,
+                                           ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ByteReport)]),
+    "scute_predict_time": (ctypes.c_int, [ctypes.POINTER(ByteReport), ctypes.c_double, ctypes.c_double,
+                                          ctypes.c_double, ctypes.POINTER(ctypes.c_double)]),
     "scute_launch_count": (ctypes.c_int64, [ctypes.c_void_p]),
     "scute_timing_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_timing_reset": (ctypes.c_int, [ctypes.c_void_p]),
@@ -115,6 +121,8 @@ _SIGS = {
     "scute_debug_fail_alloc": (None, [ctypes.c_int]),
     "scute_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]),
+    "scute_timing_kinds": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int)]),
 }
 
 
@@ -289,6 +297,45 @@ def scute_predict_bytes(ctx, ids_host, n, layer, out_dtype) -> dict:
     return rep.as_dict()
 
 
+def scute_byte_model_batch(layers, ids_host, n) -> dict:
+    """``layers``: sequence of BmLayer (one per call of the batch)."""
+    arr = (BmLayer * max(1, len(layers)))(*layers)
+    rep = ByteReport()
+    code = load().scute_byte_model_batch(arr, len(layers), ptr(ids_host), n, ctypes.byref(rep))
+    if code != 0:
+        raise ScuteError(code, "scute_byte_model_batch failed")
+    return rep.as_dict()
+
+
+def scute_predict_batch(ctx, layers, ids_host, n, out_dtype) -> dict:
+    """Launch list of a batched call over the given layer ids."""
+    arr = (Call * max(1, len(layers)))()
+    for i, layer in enumerate(layers):
+        arr[i].layer = layer
+    rep = ByteReport()
+    _check(ctx, load().scute_predict_batch(ctx, arr, len(layers), ptr(ids_host), n, out_dtype, ctypes.byref(rep)))
+    return rep.as_dict()
+
+
+def scute_predict_time(report: dict, hbm_gbs: float, tensor_tflops: float, launch_us: float) -> float:
+    """Predicted microseconds of a launch list (a report dict as returned above)."""
+    rep = ByteReport()
+    ks = report["kernels"]
+    if len(ks) > BM_MAX_KERNELS:
+        raise ValueError("too many launches")
+    rep.n_kernels = len(ks)
+    for i, (name, b, f) in enumerate(ks):
+        rep.name[i].value = name.encode()[:23]
+        rep.bytes[i] = int(b)
+        rep.flops[i] = int(f)
+    us = ctypes.c_double()
+    code = load().scute_predict_time(ctypes.byref(rep), float(hbm_gbs), float(tensor_tflops), float(launch_us),
+                                     ctypes.byref(us))
+    if code != 0:
+        raise ScuteError(code, "scute_predict_time failed")
+    return us.value
+
+
 def scute_launch_count(ctx) -> int:
     return load().scute_launch_count(ctx)
 
@@ -319,6 +366,16 @@ def scute_timing_read(ctx, max_slots: int = TIMING_SLOTS) -> list:
     n = ctypes.c_int()
     _check(ctx, load().scute_timing_read(ctx, buf, max_slots, ctypes.byref(n)))
     return [float(buf[i]) for i in range(n.value)]
+
+
+KIND_NAMES = ("step", "index", "rotate", "base_gemm", "lowrank", "vera_shrink", "vera_expand")
+
+
+def scute_timing_kinds(ctx, max_slots: int = TIMING_SLOTS) -> list:
+    buf = (ctypes.c_int * max_slots)()
+    n = ctypes.c_int()
+    _check(ctx, load().scute_timing_kinds(ctx, buf, max_slots, ctypes.byref(n)))
+    return [KIND_NAMES[buf[i]] for i in range(n.value)]
 
 
 from .context import Context  # noqa: E402,F401

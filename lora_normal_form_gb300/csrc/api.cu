@@ -126,6 +126,35 @@ bool layer_ok(const scute_ctx *c, int layer) {
 
 void count_launch(scute_ctx *c, int k) { c->launches += k; }
 
+// Timing ring (scute_timing_*): while enabled, every launch (or launch pair)
+// of the hot path is bracketed by an event pair on its stream, tagged with its
+// kind.  Event records made while the stream is being captured become graph
+// nodes, re-recorded on every replay.
+struct TimedLaunch {
+    scute_ctx *c;
+    cudaStream_t st;
+    int slot = -1;
+    unsigned flags = cudaEventRecordDefault;
+    cudaError_t begin() {
+        if (!c->timing) return cudaSuccess;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(st, &cs);
+        if (e != cudaSuccess) return e;
+        if (cs == cudaStreamCaptureStatusActive) flags = cudaEventRecordExternal;
+        slot = c->t_next;
+        return cudaEventRecordWithFlags(c->ev[slot][0], st, flags);
+    }
+    cudaError_t end(int kind) {
+        if (!c->timing || slot < 0) return cudaSuccess;
+        const cudaError_t e = cudaEventRecordWithFlags(c->ev[slot][1], st, flags);
+        c->ev_kind[slot] = kind;
+        c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
+        if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
+        slot = -1;
+        return e;
+    }
+};
+
 }  // namespace
 
 extern "C" {
@@ -178,6 +207,7 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               dev_malloc((void **)&c->d_aid, sizeof(int) * max_tokens) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_start, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
+              dev_malloc((void **)&c->d_seg_unit, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
               dev_malloc((void **)&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
               cudaMemset(c->d_meta, 0, sizeof(IndexMeta)) == cudaSuccess &&
               dev_malloc((void **)&c->d_status, sizeof(int)) == cudaSuccess &&
@@ -211,7 +241,7 @@ void scute_destroy(scute_ctx *c) {
     }
     for (auto &a : c->adapters)
         if (a.storage) cudaFree(a.storage);
-    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid,
+    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
                     c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_v, c->step_part,
                     c->step_sync, c->step_hx, c->step_hout};
@@ -708,21 +738,11 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
     if ((size_t)(units + tile + G) * 2 * 128 * BN > c->step_part_floats)
         return fail(c, SCUTE_ERR_UNSUPPORTED, "partial-tile workspace too small for this batch");
     if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
-    const int slot = c->t_next;
-    unsigned ev_flags = cudaEventRecordDefault;
-    if (c->timing) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        CU_TRY(c, cudaStreamIsCapturing(st, &cs));
-        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
-        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][0], st, ev_flags));
-    }
+    TimedLaunch tl{c, st};
+    CU_TRY(c, tl.begin());
     cudaGetLastError();
     CU_TRY(c, launch_step(a, st));
-    if (c->timing) {
-        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][1], st, ev_flags));
-        c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
-        if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
-    }
+    CU_TRY(c, tl.end(SCUTE_KIND_STEP));
     count_launch(c, 1);
     return SCUTE_OK;
 }
@@ -756,18 +776,29 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     const bool vera_on = L.rv > 0 && L.n_vera > 0;
     // Other batches (fp32 contexts, or more than STEP_MAX_TOKENS tokens): one
     // launch per step.
+    TimedLaunch tl{c, st};
     {
         // 1. token indexing
+        CU_TRY(c, tl.begin());
         CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
-                               c->d_seg_aid, c->d_meta, c->d_status, st));
+                               c->d_seg_aid, c->d_meta, c->d_status, st, c->d_seg_unit));
+        CU_TRY(c, tl.end(SCUTE_KIND_INDEX));
         ++k;
         // 2. rotation prologue into the sorted token operand
+        CU_TRY(c, tl.begin());
         CU_TRY(c, launch_gather_rotate(f32, x, L.d_in, nn, c->d_perm, c->d_aid, slots, c->xs, L.kdim, st,
                                        c->pdl));
+        CU_TRY(c, tl.end(SCUTE_KIND_ROTATE));
         ++k;
     }
     // 3. base GEMM with the s / b epilogue
     const bool tok_on_p = nn > 256;
+    // owned low-rank term: units of SEG_UNIT_ROWS rows of every segment;
+    // there are at most n / SEG_UNIT_ROWS + (segments) of them, and at most
+    // one segment per registered adapter plus the base rows
+    int reg = 0;
+    for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
+    const int unit_bound = (nn + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS + (reg + 1 < nn ? reg + 1 : nn);
     GemmArgs g;
     memset(&g, 0, sizeof(g));
     g.mapP = tok_on_p ? L.mapXs : L.mapW;
@@ -800,31 +831,17 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         return fail(c, SCUTE_ERR_UNSUPPORTED, "K-split workspace too small for this launch");
     g.part = c->gpart;
     g.part_stride = (long long)p.bn * 128 * (g.vera_kb ? 2 : 1);
-    const int slot = c->t_next;
-    unsigned ev_flags = cudaEventRecordDefault;
-    if (c->timing) {
-        // inside stream capture an event record must become a graph node
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        CU_TRY(c, cudaStreamIsCapturing(st, &cs));
-        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
-        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][0], st, ev_flags));
-    }
+    CU_TRY(c, tl.begin());
     CU_TRY(c, launch_gemm(g, p, st, c->pdl));
-    if (c->timing) {
-        CU_TRY(c, cudaEventRecordWithFlags(c->ev[slot][1], st, ev_flags));
-        c->t_next = (slot + 1) % SCUTE_TIMING_SLOTS;
-        if (c->t_used < SCUTE_TIMING_SLOTS) ++c->t_used;
-    }
+    CU_TRY(c, tl.end(SCUTE_KIND_BASE_GEMM));
     ++k;
     // 4. owned low-rank shrink / expand
     if (L.n_lr > 0) {
-        int bound = nn;
-        int reg = 0;
-        for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
-        if (reg + 1 < bound) bound = reg + 1;
-        CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, nn, bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
-                                 c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
+        CU_TRY(c, tl.begin());
+        CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, unit_bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
+                                 c->d_seg_unit, c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
                                  lr_rmax));
+        CU_TRY(c, tl.end(SCUTE_KIND_LOWRANK));
         k += 2;
     }
     // 5. VeRA: shared shrink then shared expand over the VeRA rows only
@@ -855,7 +872,9 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         v.part = c->gpart;
         v.part_stride = (long long)pv.bn * 128;
         v.n_ft = tok_on_p ? (L.rv + pv.bn - 1) / pv.bn : (L.rv + 127) / 128;
+        CU_TRY(c, tl.begin());
         CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
+        CU_TRY(c, tl.end(SCUTE_KIND_VERA_SHRINK));
 
         GemmArgs e = v;
         e.mapP = tok_on_p ? L.mapU : L.mapBsh;
@@ -873,7 +892,9 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         e.part = c->gpart;
         e.part_stride = (long long)pe.bn * 128;
         e.n_ft = tok_on_p ? (L.d_out + pe.bn - 1) / pe.bn : (L.d_out + 127) / 128;
+        CU_TRY(c, tl.begin());
         CU_TRY(c, launch_gemm(e, pe, st, c->pdl));
+        CU_TRY(c, tl.end(SCUTE_KIND_VERA_EXPAND));
         k += 2;
     }
     count_launch(c, k);
@@ -1045,6 +1066,14 @@ scute_status scute_timing_read(scute_ctx *c, float *ms, int max, int *n_out) {
     CU_TRY(c, cudaDeviceSynchronize());
     int m = c->t_used < max ? c->t_used : max;
     for (int i = 0; i < m; ++i) CU_TRY(c, cudaEventElapsedTime(&ms[i], c->ev[i][0], c->ev[i][1]));
+    *n_out = m;
+    return SCUTE_OK;
+}
+
+scute_status scute_timing_kinds(const scute_ctx *c, int *kinds, int max, int *n_out) {
+    if (!c || !kinds || !n_out) return SCUTE_ERR_ARG;
+    int m = c->t_used < max ? c->t_used : max;
+    for (int i = 0; i < m; ++i) kinds[i] = c->ev_kind[i];
     *n_out = m;
     return SCUTE_OK;
 }

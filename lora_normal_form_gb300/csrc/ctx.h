@@ -60,6 +60,7 @@ struct scute_ctx {
     Slot *d_slots = nullptr;
     int8_t *d_method = nullptr;
     int *d_perm = nullptr, *d_aid = nullptr, *d_seg_start = nullptr, *d_seg_aid = nullptr;
+    int *d_seg_unit = nullptr;   // work units of the segmented low-rank kernels
     IndexMeta *d_meta = nullptr;
     int *d_status = nullptr;
     int *d_err = nullptr;
@@ -94,6 +95,7 @@ struct scute_ctx {
     int64_t launches = 0;
     bool timing = false;
     cudaEvent_t ev[SCUTE_TIMING_SLOTS][2];
+    int ev_kind[SCUTE_TIMING_SLOTS] = {};
     bool ev_made = false;
     int t_next = 0, t_used = 0;
     char err[512];

@@ -115,10 +115,10 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
                    int lr_rmax = 0);
 cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl);
 
-// K splits of the owned low-rank shrink: at most KS_MAX chunks of a multiple
-// of 256 elements each.
+// K splits of the owned low-rank shrink: chunks of about 2048 elements, at
+// most KS_MAX of them, each a multiple of 256 elements.
 inline int lowrank_ks(int d_in, int *kchunk_out) {
-    int ks = (d_in + 511) / 512;
+    int ks = (d_in + 2047) / 2048;
     if (ks > KS_MAX) ks = KS_MAX;
     int kchunk = (d_in + ks - 1) / ks;
     kchunk = (kchunk + 255) / 256 * 256;
@@ -229,19 +229,24 @@ size_t step_smem_bytes(int bn, int stages, int rmax);
 cudaError_t launch_step(const StepArgs &a, cudaStream_t st);
 
 // ---------------------------------------------------------------- other kernels
+// Token indexing (one CTA).  seg_unit (optional, n_seg + 1 ints): the
+// segmented low-rank kernels' work units, every segment cut into chunks of
+// SEG_UNIT_ROWS sorted rows; seg_unit[s] counts the chunks before segment s.
+constexpr int SEG_UNIT_ROWS = 32;
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
-                         int *status, cudaStream_t st);
+                         int *status, cudaStream_t st, int *seg_unit = nullptr);
 
 cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const int *perm,
                                  const int *aid_s, const Slot *slots, void *xs, int kdim,
                                  cudaStream_t st, bool pdl);
 
-cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int n, int seg_bound,
-                           const int *perm, const int *seg_start, const int *seg_aid,
-                           const IndexMeta *meta, const Slot *slots, float *v_part,
-                           int max_tokens, void *out, int out_f32, cudaStream_t st, bool pdl,
-                           int max_rank);
+// Segmented owned low-rank shrink and expand over the units of launch_index
+// (unit_bound: a host-side bound on their number).
+cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int unit_bound, const int *perm,
+                           const int *seg_start, const int *seg_aid, const int *seg_unit,
+                           const IndexMeta *meta, const Slot *slots, float *v_part, int max_tokens, void *out,
+                           int out_f32, cudaStream_t st, bool pdl, int max_rank);
 
 // registration-time kernels
 cudaError_t launch_transpose_w(bool f32, const void *W, int rows, int cols, void *Wt, int kdim,

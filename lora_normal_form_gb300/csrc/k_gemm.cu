@@ -758,8 +758,10 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
     GemmPlan p{};
     p.tf32 = tf32 ? 1 : 0;
     if (tok_on_p) {
-        // prefill orientation: 128 tokens x 256 features, persistent tiles
-        p.bn = 256;
+        // prefill orientation: 128 tokens x 256 features, persistent tiles; a
+        // narrow product (the VeRA shrink to the shared rank) takes 64-feature
+        // tiles, so that more CTAs share its K loop
+        p.bn = n_feat <= 256 ? 64 : 256;
         p.splits = 1;
         p.stages = 4;
         const int tiles = ((n_tok + TILE_M - 1) / TILE_M) * ((n_feat + p.bn - 1) / p.bn);

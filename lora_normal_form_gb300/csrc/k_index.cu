@@ -11,6 +11,7 @@
 //   aid_s[i]       adapter of sorted row i (-1 = base only)
 //   seg_start/aid  maximal runs of one key
 //   meta           rows, first row and segments per method
+//   seg_unit       (optional) chunks of SEG_UNIT_ROWS rows before each segment
 // Ids that name no registered adapter become base-only rows and set
 // STATUS_BAD_ADAPTER.
 //
@@ -108,7 +109,8 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
 
 __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, const int8_t *method_tab,
                                                      int A, int *perm, int *aid_s, int *seg_start,
-                                                     int *seg_aid, IndexMeta *meta, int *status) {
+                                                     int *seg_aid, IndexMeta *meta, int *status,
+                                                     int *seg_unit) {
     extern __shared__ uint32_t sm[];
     uint32_t *bufA = sm;
     uint32_t *bufB = sm + n;
@@ -160,9 +162,24 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
             ++s;
         }
     }
+    if (tid == 0) seg_start[total] = n;
     __syncthreads();
+    if (seg_unit) {
+        // work units of the segmented kernels: each segment cut into chunks of
+        // SEG_UNIT_ROWS rows; seg_unit[s] = chunks of the segments before s
+        const int per_s = (total + blockDim.x - 1) / blockDim.x;
+        const int s0 = min(total, tid * per_s), s1 = min(total, s0 + per_s);
+        int u = 0;
+        for (int q = s0; q < s1; ++q) u += (seg_start[q + 1] - seg_start[q] + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS;
+        int tot_u = 0;
+        int ex = block_excl_scan(u, s_warp, &tot_u);
+        for (int q = s0; q < s1; ++q) {
+            seg_unit[q] = ex;
+            ex += (seg_start[q + 1] - seg_start[q] + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS;
+        }
+        if (tid == 0) seg_unit[total] = tot_u;
+    }
     if (tid == 0) {
-        seg_start[total] = n;
         meta->n_seg = total;
         int off = 0;
         for (int r = 0; r < N_RANKS; ++r) {
@@ -179,7 +196,7 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
 
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
-                         int *status, cudaStream_t st) {
+                         int *status, cudaStream_t st, int *seg_unit) {
     static std::atomic<unsigned long long> attr_done{0};
     {
         const cudaError_t e = allow_max_dynamic_smem(index_kernel, attr_done);
@@ -198,7 +215,7 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, index_kernel, ids, n, method_tab, max_adapters, perm, aid_s,
-                              seg_start, seg_aid, meta, status);
+                              seg_start, seg_aid, meta, status, seg_unit);
 }
 
 }  // namespace scute

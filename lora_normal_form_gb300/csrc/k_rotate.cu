@@ -8,11 +8,11 @@
 // compute the remaining slots?").  Rows of every other adapter are copied
 // unchanged, so the GEMM reads one contiguous token operand in sorted order.
 //
-// Grid: x = 256-column chunk (8 blocks of 32), y = run of sorted rows.  Rows
-// of one adapter are contiguous after indexing, so a CTA stages that adapter's
-// 8 blocks of R in shared memory once and reuses them for every row of the run.
-// An fp32 context writes each value as three tf32 parts [hi | hi | lo] for the
-// split-precision GEMM (hi = tf32(v), lo = v - hi).
+// fp32 contexts (gather_rotate_kernel): x = 256-column chunk (8 blocks of 32),
+// y = run of sorted rows; a CTA stages its adapter's 8 blocks of R in shared
+// memory once per run of one adapter, and writes each value as three tf32
+// parts [hi | hi | lo] for the split-precision GEMM (hi = tf32(v), lo = v - hi).
+// bf16 contexts: gather_rotate_bf16_kernel below.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -82,6 +82,86 @@ __global__ void __launch_bounds__(256) gather_rotate_kernel(const T *__restrict_
     }
 }
 
+// bf16 contexts: one warp per sorted row and 256-column chunk, lane l moving
+// columns [8l, 8l + 8) with one 16-byte load and store.  A rotated row's lane
+// computes its 8 outputs of one 32x32 block: the block's 32 inputs come from
+// the block's 4 lanes by shuffle, and output column j reads row j of the
+// block-transposed copy of R (32 contiguous bf16) through L1, where the rows of
+// one adapter that the same CTA handles find it again.  No shared memory and
+// no barrier: every row is independent.
+__global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int d_in,
+                                                                 int n, const int *__restrict__ perm,
+                                                                 const int *__restrict__ aid_s,
+                                                                 const Slot *__restrict__ slots,
+                                                                 __nv_bfloat16 *xs, int kdim) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = blockIdx.x * 256 + lane * 8;
+    const bool colok = col < d_in;     // d_in is a multiple of 32: a block's 4 lanes agree
+    const int row0 = blockIdx.y * 32 + warp * 4;
+    uint4 xv[4];
+    int ad[4];
+    // every load of the warp's 4 rows is issued before any is used
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = row0 + r;
+        ad[r] = i < n ? aid_s[i] : -2;
+        xv[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < n && colok) xv[r] = *reinterpret_cast<const uint4 *>(x + (size_t)perm[i] * d_in + col);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = row0 + r;
+        if (i >= n) break;   // uniform across the warp
+        const __nv_bfloat16 *Rt =
+            ad[r] >= 0 ? reinterpret_cast<const __nv_bfloat16 *>(slots[ad[r]].Rt) : nullptr;
+        uint4 o = xv[r];
+        if (Rt != nullptr) {
+            // the 32 inputs of this lane's block, as 16 bf16 pairs
+            uint32_t xin[16];
+            const uint32_t *mine = reinterpret_cast<const uint32_t *>(&xv[r]);
+            const int base = lane & ~3;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                for (int w = 0; w < 4; ++w) xin[s4 * 4 + w] = __shfl_sync(0xffffffffu, mine[w], base + s4);
+            float xf[32];
+#pragma unroll
+            for (int p = 0; p < 16; ++p) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xin[p]));
+                xf[2 * p] = f.x;
+                xf[2 * p + 1] = f.y;
+            }
+            if (colok) {
+                const int b = col / OFT_BLK, j0 = col % OFT_BLK;
+                const uint4 *Rrow = reinterpret_cast<const uint4 *>(Rt + ((size_t)b * OFT_BLK + j0) * OFT_BLK);
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 u = __ldg(Rrow + e * 4 + q);
+                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float2 f = __bfloat1622float2(h[t]);
+                            acc = fmaf(xf[q * 8 + 2 * t], f.x, acc);
+                            acc = fmaf(xf[q * 8 + 2 * t + 1], f.y, acc);
+                        }
+                    }
+                    y[e] = acc;
+                }
+                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) h[t] = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);
+            }
+        }
+        if (colok) *reinterpret_cast<uint4 *>(xs + (size_t)i * kdim + col) = o;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const int *perm,
@@ -100,8 +180,9 @@ cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const
     if (f32)
         return cudaLaunchKernelEx(&cfg, gather_rotate_kernel<float>, (const float *)x, d_in, n, perm,
                                   aid_s, slots, (float *)xs, kdim, rows);
-    return cudaLaunchKernelEx(&cfg, gather_rotate_kernel<__nv_bfloat16>, (const __nv_bfloat16 *)x, d_in,
-                              n, perm, aid_s, slots, (__nv_bfloat16 *)xs, kdim, rows);
+    cfg.gridDim = dim3((unsigned)((d_in + 255) / 256), (unsigned)((n + 31) / 32), 1);
+    return cudaLaunchKernelEx(&cfg, gather_rotate_bf16_kernel, (const __nv_bfloat16 *)x, d_in, n, perm, aid_s,
+                              slots, (__nv_bfloat16 *)xs, kdim);
 }
 
 }  // namespace scute

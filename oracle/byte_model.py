@@ -19,23 +19,21 @@ from __future__ import annotations
 
 
 def lowrank_ks(d_in: int) -> int:
-    """K splits of the owned low-rank shrink: ceil(d_in / 512) chunks, at most
+    """K splits of the owned low-rank shrink: ceil(d_in / 2048) chunks, at most
     8, each a multiple of 256 elements (the chunk count after rounding)."""
-    ks = min(8, -(-d_in // 512))
+    ks = min(8, -(-d_in // 2048))
     chunk = -(-d_in // ks)
     chunk = -(-chunk // 256) * 256
     return -(-d_in // chunk)
 
 
-def call_bytes(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dtype: str,
-               out_dtype: str, lowrank_launched: bool, vera_launched: bool) -> dict:
+def _layer_counts(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dtype: str,
+                  out_dtype: str) -> dict:
+    """Rows, distinct adapters and live-tensor bytes of one layer's call."""
     E = 4 if dtype == "fp32" else 2
-    Eo = 4 if out_dtype == "fp32" else 2
-    kd = 3 * d_in if dtype == "fp32" else d_in
-    rv = shared_rank
-    krv = 3 * rv if dtype == "fp32" else rv
-    n = len(ids)
-
+    c = {"E": E, "Eo": 4 if out_dtype == "fp32" else 2, "kd": 3 * d_in if dtype == "fp32" else d_in,
+         "rv": shared_rank, "krv": 3 * shared_rank if dtype == "fp32" else shared_rank,
+         "n": len(ids), "d_in": d_in, "d_out": d_out}
     seen = []
     has_base = False
     n_lr = lr_rank_rows = n_v = n_rot = 0
@@ -54,7 +52,6 @@ def call_bytes(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dty
             n_rot += 1
         if a not in seen:
             seen.append(a)
-
     live = R_b = sb_b = A_b = B_b = d_b = e_b = 0
     for a in seen:
         ad = adapters[a]
@@ -72,59 +69,100 @@ def call_bytes(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dty
             A_b += ad["rank"] * d_in * E
             B_b += ad["rank"] * d_out * E
         if ad["vera"]:
-            live += 4 * rv
-            d_b += 4 * rv
+            live += 4 * shared_rank
+            d_b += 4 * shared_rank
             if ad["vera_e"]:
                 live += 4 * d_out
                 e_b += 4 * d_out
-    segments = len(seen) + (1 if has_base else 0)
+    c.update(seen=seen, segments=len(seen) + (1 if has_base else 0), n_lr=n_lr, lr_rank_rows=lr_rank_rows,
+             n_v=n_v, n_rot=n_rot, live=live, R_b=R_b, sb_b=sb_b, A_b=A_b, B_b=B_b, d_b=d_b, e_b=e_b)
+    c["shared"] = (d_in + d_out) * shared_rank * E if n_v else 0
+    c["W"] = d_in * d_out * E
+    # W once, each distinct adapter's live tensors once, the shared pair once
+    # when a VeRA token is present, x read, out written (ids counted by the caller)
+    c["alg_no_ids"] = c["W"] + live + c["shared"] + c["n"] * d_in * E + c["n"] * d_out * c["Eo"]
+    # every term of the normal form over the batch: base GEMM, rotation,
+    # owned shrink and expand, VeRA shrink and expand (2 flops per multiply-add)
+    c["flops"] = (2 * c["n"] * d_in * d_out + 2 * n_rot * d_in * 32 + 2 * lr_rank_rows * (d_in + d_out)
+                  + 2 * n_v * shared_rank * (d_in + d_out))
+    return c
 
-    # bf16 calls of at most 128 tokens follow the fused decode plan (one
-    # prologue launch and one GEMM launch); others launch one kernel per step
-    fused = dtype != "fp32" and n <= 128
-    index_out = 8 * n + 4 * (segments + 1) + 4 * segments + 88
-    if fused:
-        shA = rv * d_in * E if n_v else 0
-        shB = d_out * rv * E if n_v else 0
-        kernels = [
-            # ids; x once; R, A', shared A, d once each; x', v, U and the index out
-            ("prep", 4 * n + n * d_in * E + R_b + A_b + shA + d_b + n * kd * E + lr_rank_rows * 4
-             + n_v * rv * E + index_out,
-             2 * n_rot * d_in * 32 + 2 * lr_rank_rows * d_in + 2 * n_v * rv * d_in),
-            # W, x', s/b, B', v, shared B, U, e, perm/ids, out
-            ("base_gemm", d_out * kd * E + n * kd * E + sb_b + B_b + lr_rank_rows * 4 + shB + n_v * rv * E
-             + e_b + 8 * n + n * d_out * Eo,
-             2 * n * kd * d_out + 2 * lr_rank_rows * d_out + 2 * n_v * rv * d_out),
-        ]
+
+def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool) -> list:
+    """Launches of one layer's call on the per-kernel plan, (name, bytes, flops)."""
+    n, E, Eo, kd, d_in, d_out = c["n"], c["E"], c["Eo"], c["kd"], c["d_in"], c["d_out"]
+    rv, krv = c["rv"], c["krv"]
+    index_out = 8 * n + 4 * (c["segments"] + 1) + 4 * c["segments"] + 88
+    kernels = [
+        # ids in; perm and sorted ids out; segment table; 22-int summary
+        ("index", 4 * n + index_out, 0),
+        # x in, perm/ids in, R of each distinct rotating adapter, x' out
+        ("rotate", n * d_in * E + 8 * n + c["R_b"] + n * kd * E, 2 * c["n_rot"] * d_in * 32),
+        # W, x', s/b vectors, perm/ids, out
+        ("base_gemm", d_out * kd * E + n * kd * E + c["sb_b"] + 8 * n + n * d_out * Eo, 2 * n * kd * d_out),
+    ]
+    if lowrank_launched:
+        ks = lowrank_ks(d_in)
+        kernels.append(("lr_shrink", c["n_lr"] * d_in * E + c["A_b"] + ks * c["lr_rank_rows"] * 4,
+                        2 * c["lr_rank_rows"] * d_in))
+        kernels.append(("lr_expand", ks * c["lr_rank_rows"] * 4 + c["B_b"] + 2 * c["n_lr"] * d_out * Eo,
+                        2 * c["lr_rank_rows"] * d_out))
+    if vera_launched:
+        n_v = c["n_v"]
+        shA = rv * kd * E if n_v else 0
+        shB = d_out * krv * E if n_v else 0
+        kernels.append(("vera_shrink", n_v * kd * E + shA + c["d_b"] + n_v * krv * E, 2 * n_v * rv * kd))
+        kernels.append(("vera_expand", n_v * krv * E + shB + c["e_b"] + 2 * n_v * d_out * Eo,
+                        2 * n_v * krv * d_out))
+    return kernels
+
+
+def batch_bytes(ids, layers: list, dtype: str, out_dtype: str) -> dict:
+    """Launch list and algorithmic bytes of one batched call over ``layers``
+    (each a dict with keys adapters, d_in, d_out, shared_rank,
+    lowrank_launched, vera_launched) that read the same ids.
+
+    A bf16 batch of at most 128 tokens is one launch over every layer; its
+    bytes are what crosses that launch: the ids once and every layer's W, live
+    adapter tensors, shared pair, x and out.  Otherwise every layer follows
+    the per-kernel plan in turn."""
+    n = len(ids)
+    cs = [_layer_counts(ids, L["adapters"], L["d_in"], L["d_out"], L["shared_rank"], dtype, out_dtype)
+          for L in layers]
+    alg = 4 * n + sum(c["alg_no_ids"] for c in cs)
+    if dtype != "fp32" and n <= 128:
+        kernels = [("step", alg, sum(c["flops"] for c in cs))]
     else:
-        kernels = [
-            # ids in; perm and sorted ids out; segment table; 22-int summary
-            ("index", 4 * n + index_out, 0),
-            # x in, perm/ids in, R of each distinct rotating adapter, x' out
-            ("rotate", n * d_in * E + 8 * n + R_b + n * kd * E, 2 * n_rot * d_in * 32),
-            # W, x', s/b vectors, perm/ids, out
-            ("base_gemm", d_out * kd * E + n * kd * E + sb_b + 8 * n + n * d_out * Eo, 2 * n * kd * d_out),
-        ]
-        if lowrank_launched:
-            ks = lowrank_ks(d_in)
-            kernels.append(("lr_shrink", n_lr * d_in * E + A_b + ks * lr_rank_rows * 4, 2 * lr_rank_rows * d_in))
-            kernels.append(("lr_expand", ks * lr_rank_rows * 4 + B_b + 2 * n_lr * d_out * Eo,
-                            2 * lr_rank_rows * d_out))
-        if vera_launched:
-            shA = rv * kd * E if n_v else 0
-            shB = d_out * krv * E if n_v else 0
-            kernels.append(("vera_shrink", n_v * kd * E + shA + d_b + n_v * krv * E, 2 * n_v * rv * kd))
-            kernels.append(("vera_expand", n_v * krv * E + shB + e_b + 2 * n_v * d_out * Eo,
-                            2 * n_v * krv * d_out))
-    shared = (d_in + d_out) * rv * E if n_v else 0
-    W = d_in * d_out * E
+        kernels = []
+        for L, c in zip(layers, cs):
+            kernels += _per_kernel_plan(c, L["lowrank_launched"], L["vera_launched"])
     return {
         "kernels": kernels,
-        "algorithmic_bytes": W + live + shared + n * d_in * E + n * d_out * Eo + 4 * n,
-        "adapter_bytes": live + shared,
-        "base_weight_bytes": W,
-        "distinct_adapters": len(seen),
+        "algorithmic_bytes": alg,
+        "adapter_bytes": sum(c["live"] + c["shared"] for c in cs),
+        "base_weight_bytes": sum(c["W"] for c in cs),
+        "distinct_adapters": len(cs[0]["seen"]),
     }
+
+
+def call_bytes(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, dtype: str,
+               out_dtype: str, lowrank_launched: bool, vera_launched: bool) -> dict:
+    """One call of one layer: a batch of one."""
+    return batch_bytes(ids, [{"adapters": adapters, "d_in": d_in, "d_out": d_out, "shared_rank": shared_rank,
+                              "lowrank_launched": lowrank_launched, "vera_launched": vera_launched}],
+                       dtype, out_dtype)
+
+
+def predict_time_us(kernels, hbm_gbs: float, tensor_tflops: float, launch_us: float) -> float:
+    """The article's time model, launch by launch: bytes / bandwidth plus one
+    launch cost per launch; a launch bound by arithmetic instead takes
+    flops / tensor peak (dropped when tensor_tflops <= 0)."""
+    t = 0.0
+    for _, b, f in kernels:
+        t_mem = b / (hbm_gbs * 1e3)
+        t_math = f / (tensor_tflops * 1e6) if tensor_tflops > 0 else 0.0
+        t += max(t_mem, t_math)
+    return t + launch_us * len(kernels)
 
 
 def adapter_slots_after_fold(method: str, raw_slots, rank: int) -> dict:

@@ -96,6 +96,10 @@ CASES = [
     ("decode_small_nf", lambda: WL.with_nf_adapters(WL.decode_mixed(n=50, shapes=WL.SMALL_PROJ, proj=("q", "down"))), "down", "bf16"),
     ("decode_llama_k", lambda: WL.decode_mixed(), "k", "bf16"),
     ("scaling", lambda: WL.scaling_ia3_vera(), "up", "bf16"),
+    ("prefill_small_fused_expand", lambda: WL.prefill_mixed(n_req=6, lo=40, hi=200, shapes=WL.SMALL_PROJ,
+                                                            proj=("q", "k", "up", "down")), "up", "bf16"),
+    ("prefill_small_rank64", lambda: WL.prefill_mixed(n_req=6, lo=40, hi=200, rank=64, shapes=WL.SMALL_PROJ,
+                                                      proj=("q", "k", "up", "down")), "q", "fp32"),
 ]
 
 
@@ -146,3 +150,65 @@ def test_byte_model_rejects_bad_arguments(lib):
                      vera_launched=0, max_adapters=1, adapters=ctypes.cast(arr, ctypes.POINTER(lib.BmAdapter)))
     with pytest.raises(lib.ScuteError):
         lib.scute_byte_model(bl, np.zeros(1, np.int32), 1)
+
+
+def test_batch_byte_model_matches_oracle(lib):
+    """A batched call over several layers (the decode workload's six
+    projections, the same layer twice, and a batch above the decode step's
+    token limit): the library's launch list equals the oracle's."""
+    for w, names, out_dtype in [
+        (WL.decode_mixed(), ("q", "k", "v", "gate", "up", "down"), "bf16"),
+        (WL.decode_mixed(n=50, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down")), ("q", "up", "q"), "fp32"),
+        (WL.decode_mixed(n=200, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down")), ("k", "down"), "bf16"),
+    ]:
+        import ctypes
+        A = max(a.id for a in w.adapters) + 3
+        keep = []
+        layers, ref_layers = [], []
+        for name in names:
+            L, ads, lowrank, vera = _bm_inputs(w, name, out_dtype)
+            arr = (lib.BmAdapter * A)()
+            for i in range(A):
+                arr[i].method = -1
+            for aid, v in ads.items():
+                arr[aid].method = lib.METHOD_ID[v["method"]]
+                arr[aid].rank = v["rank"]
+                arr[aid].has_s, arr[aid].has_b, arr[aid].has_R = int(v["s"]), int(v["b"]), int(v["R"])
+                arr[aid].has_vera, arr[aid].has_vera_e = int(v["vera"]), int(v["vera_e"])
+            keep.append(arr)
+            layers.append(lib.BmLayer(dtype=lib.FP32 if w.dtype == "fp32" else lib.BF16,
+                                      out_dtype=lib.FP32 if out_dtype == "fp32" else lib.BF16,
+                                      d_in=L.d_in, d_out=L.d_out, shared_rank=L.shared_rank,
+                                      lowrank_launched=int(lowrank), vera_launched=int(vera), max_adapters=A,
+                                      adapters=ctypes.cast(arr, ctypes.POINTER(lib.BmAdapter))))
+            ref_layers.append({"adapters": ads, "d_in": L.d_in, "d_out": L.d_out, "shared_rank": L.shared_rank,
+                               "lowrank_launched": lowrank, "vera_launched": vera})
+        ids = w.ids.copy()
+        ids[1] = -1
+        got = lib.scute_byte_model_batch(layers, np.ascontiguousarray(ids, np.int32), int(ids.size))
+        ref = OBM.batch_bytes(ids, ref_layers, w.dtype, out_dtype)
+        assert got["kernels"] == [tuple(k) for k in ref["kernels"]]
+        for k in ("algorithmic_bytes", "adapter_bytes", "base_weight_bytes", "distinct_adapters"):
+            assert got[k] == ref[k], k
+        if w.dtype != "fp32" and w.n <= 128:
+            # one launch, whose bytes are the call's algorithmic bytes
+            assert len(got["kernels"]) == 1 and got["kernels"][0][1] == got["algorithmic_bytes"]
+        # the time model: library and oracle agree
+        for bw, tf, lc in [(6794.5, 0.0, 2.0), (6794.5, 1846.4, 1.3)]:
+            t = lib.scute_predict_time(got, bw, tf, lc)
+            assert abs(t - OBM.predict_time_us(ref["kernels"], bw, tf, lc)) <= 1e-9 * max(1.0, t)
+
+
+def test_time_model_hand_example(lib):
+    """Two launches counted by hand: 1e6 bytes at 1000 GB/s is 1 us; 2e9 flops
+    at 1000 TFLOP/s is 2 us, so the first launch takes max(1, 2) = 2 us; the
+    second moves 3e6 bytes (3 us) and does no arithmetic; plus 2 launches of
+    0.5 us: 2 + 3 + 1 = 6 us.  Without the flops term (the article's form):
+    1 + 3 + 1 = 5 us."""
+    rep = {"kernels": [("a", 1_000_000, 2_000_000_000), ("b", 3_000_000, 0)]}
+    assert abs(lib.scute_predict_time(rep, 1000.0, 1000.0, 0.5) - 6.0) <= 1e-12
+    assert abs(lib.scute_predict_time(rep, 1000.0, 0.0, 0.5) - 5.0) <= 1e-12
+    assert abs(OBM.predict_time_us(rep["kernels"], 1000.0, 1000.0, 0.5) - 6.0) <= 1e-12
+    assert abs(OBM.predict_time_us(rep["kernels"], 1000.0, 0.0, 0.5) - 5.0) <= 1e-12
+    with pytest.raises(lib.ScuteError):
+        lib.scute_predict_time(rep, 0.0, 0.0, 0.5)

@@ -277,6 +277,22 @@ def test_rank1_and_rank64(scute):
         ctx.close()
 
 
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_many_short_segments_rank64(scute, out_dtype):
+    """200 tokens over 160 adapters with Zipf(1.0) ids, LoRA / DoRA rank 64:
+    most segments hold one or two rows (the per-kernel plan's segmented
+    low-rank kernels in their decode-like regime, and rank groups beyond 16)."""
+    n = 200
+    ids = WL.zipf_ids(5, n, 160)
+    w = WL.decode_mixed(n=n, shapes=WL.SMALL_PROJ, proj=("q", "down"), n_adapters=160, rank=64, ids=ids)
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, ("q", "down"), out_dtype)
+    assert ctx.sync_status() == 0
+    for name in ("q", "down"):
+        H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
 def test_bad_ids_become_base_and_are_reported(scute):
     w = _small_decode(n=32)
     ids = w.ids.copy()

@@ -405,3 +405,84 @@ SMALL_PROJ = {
     "up": (544, 1312, True),
     "down": (1312, 544, False),
 }
+
+
+# --------------------------------------------------------------------------
+# the same distributions drawn on a CUDA device (bench legs whose host-side
+# draws would take minutes: the 32-layer stack, the 1024-adapter scaling
+# batch).  Streams are keyed by (seed, name) as above, but the values are
+# torch's, not NumPy's: these tensors feed timings, never a parity check.
+# --------------------------------------------------------------------------
+def _seed_int(seed, *names) -> int:
+    h = hashlib.sha256(repr(("device", int(seed)) + tuple(names)).encode()).digest()
+    return int.from_bytes(h[:8], "little") & ((1 << 63) - 1)
+
+
+def device_normal(seed, name, shape, std, dtype, device, mean=0.0):
+    """N(mean, std^2) drawn on ``device``; bf16 (round-to-nearest-even from
+    float32) or float32."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(_seed_int(seed, name))
+    v = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    v.mul_(std)
+    if mean:
+        v.add_(mean)
+    return v.to(torch.bfloat16) if dtype == "bf16" else v
+
+
+def device_vector(seed, name, n, device, std=0.1):
+    """1 + N(0, std^2), float32, on ``device``."""
+    return device_normal(seed, name, (n,), std, "fp32", device, mean=1.0)
+
+
+def device_cayley_blocks(seed, name, n_blk, dtype, device, std=0.05, blk=OFT_BLOCK):
+    """Orthogonal blocks (I + S)(I - S)^-1, S skew with upper entries N(0, std),
+    drawn and solved in float64 on ``device``."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(_seed_int(seed, name))
+    up = torch.triu(torch.randn((n_blk, blk, blk), generator=g, device=device, dtype=torch.float64) * std, 1)
+    S = up - up.transpose(1, 2)
+    I = torch.eye(blk, device=device, dtype=torch.float64).expand(n_blk, blk, blk)
+    R = torch.linalg.solve((I - S).transpose(1, 2), (I + S).transpose(1, 2)).transpose(1, 2)
+    return R.to(torch.bfloat16 if dtype == "bf16" else torch.float32).contiguous()
+
+
+def device_layer_tensors(seed, L: Layer, dtype: str, device) -> dict:
+    """W [d_in, d_out] and the shared VeRA pair of one layer, on the device."""
+    t = {"W": device_normal(seed, f"W/{L.name}", (L.d_in, L.d_out), 0.02, dtype, device)}
+    if L.shared_rank:
+        t["A_sh"] = device_normal(seed, f"Ash/{L.name}", (L.d_in, L.shared_rank), 0.02, dtype, device)
+        t["B_sh"] = device_normal(seed, f"Bsh/{L.name}", (L.shared_rank, L.d_out), 0.02, dtype, device)
+    return t
+
+
+def device_adapter_tensors(seed, a: Adapter, layers: List[Layer], dtype: str, device,
+                           vec_std=0.1) -> List[Tuple[str, dict]]:
+    """One adapter's raw tensors on every layer it has, drawn on the device
+    with the distributions of ``_make_adapter``."""
+    out = []
+    by_name = {L.name: L for L in layers}
+    for lname in a.layers:
+        L = by_name[lname]
+        pre = f"ad{a.id}/{lname}"
+        t = {}
+        if a.method in ("lora", "dora"):
+            t["A"] = device_normal(seed, pre + "/A", (L.d_in, a.rank), 0.02, dtype, device)
+            t["B"] = device_normal(seed, pre + "/B", (a.rank, L.d_out), 0.02, dtype, device)
+            if a.method == "dora":
+                t["magnitude"] = device_vector(seed, pre + "/m", L.d_out, device, vec_std) * float(
+                    0.02 * np.sqrt(L.d_in))
+        elif a.method == "ia3":
+            t["l"] = device_vector(seed, pre + "/l", L.d_out, device, vec_std)
+        elif a.method == "vera":
+            t["d"] = device_vector(seed, pre + "/d", L.shared_rank, device, vec_std)
+            t["e"] = device_vector(seed, pre + "/e", L.d_out, device, vec_std)
+        elif a.method == "oft":
+            t["R"] = device_cayley_blocks(seed, pre + "/R", L.d_in // OFT_BLOCK, dtype, device)
+        else:
+            raise ValueError(a.method)
+        out.append((lname, t))
+    return out
+
