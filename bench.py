@@ -92,6 +92,7 @@ def parse():
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill leg")
     p.add_argument("--no-scaling", action="store_true", help="skip the adapter-count scaling leg")
     p.add_argument("--no-stack", action="store_true", help="skip the 32-layer stack leg")
+    p.add_argument("--no-validation", action="store_true", help="skip the time-model validation leg")
     p.add_argument("--eager-steps", type=int, default=0,
                    help="only run this many untimed batched steps of the mixed workload and exit "
                         "(a fixed launch sequence for profilers); prints no JSON line")
@@ -574,6 +575,86 @@ def stack_leg(scute, dev, flush, launch_us, steps=10):
                         "all-LoRA twin: same ids, rank-16 LoRA", "peak_gbs": hbm, "peak_kind": peak_kind, **res}
 
 
+def validation_leg(scute, dev, flush, launch_us, steps=30):
+    """The time model checked on separate-pass placements (the article's
+    validation: OFT's rotation in its own pass, DoRA's s outside the expand):
+    the six decode projections at 16, 32, 64 and 128 tokens, each placement's
+    added time predicted (extra bytes / bandwidth + extra launches x launch
+    cost) and measured (graph replays, L2 flushed), and each pass launch's own
+    time beside its prediction."""
+    import torch
+    hbm, tf, _, peak_kind = peaks()
+    w = WL.decode_mixed(n=128)
+    ctx = scute.Context("bf16", max_tokens=128, max_adapters=40, max_layers=8, device=dev.index)
+    rows = []
+    try:
+        ctx.load_workload(w)
+        stream = torch.cuda.Stream(device=dev)
+        xs = {p: torch.from_numpy(np.ascontiguousarray(w.layer(p).get("x")).view(np.int16)).to(dev)
+              .view(torch.bfloat16) for p in PROJ}
+        outs = {p: torch.empty(128, w.layer(p).d_out, dtype=torch.bfloat16, device=dev) for p in PROJ}
+        ids_all = torch.from_numpy(w.ids.copy()).to(dev)
+        for n in (16, 32, 64, 128):
+            ids = ids_all[:n]
+
+            def call():
+                ctx.linear_batch([(xs[p][:n], ctx.layer_ids[p], outs[p][:n]) for p in PROJ], ids, "bf16",
+                                 stream=stream)
+            res = {}
+            for v in (0, 1, 2, 3):
+                ctx.set_variant(v)
+                with torch.cuda.stream(stream):
+                    call()
+                torch.cuda.synchronize()
+                g = capture(call, stream)
+                graph_time(g, stream, flush, 3)
+                ms, _ = graph_time(g, stream, flush, steps)
+                # each launch of the call timed on its own (eager, event pairs)
+                ctx.timing(True)
+                per = {}
+                for _ in range(5):
+                    ctx.timing_reset()
+                    with torch.cuda.stream(stream):
+                        flush.fill_(1)
+                    call()
+                    for k, t in zip(ctx.timing_kinds(), ctx.timing_read()):
+                        per.setdefault(k, []).append(t)
+                ctx.timing(False)
+                rep = ctx.predict_batch([ctx.layer_ids[p] for p in PROJ], w.ids[:n], "bf16")
+                res[v] = {"ms": ms, "rep": rep, "kernel_ms": {k: float(np.median(t)) for k, t in per.items()}}
+                del g
+            base = res[0]
+            pred0 = scute.scute_predict_time(base["rep"], hbm, 0.0, launch_us)
+            for v, label in ((1, "rotation as its own pass"), (2, "DoRA / (IA)^3 s as its own pass"),
+                             (3, "both passes")):
+                r = res[v]
+                pred = scute.scute_predict_time(r["rep"], hbm, 0.0, launch_us)
+                added_meas = 1e3 * (r["ms"] - base["ms"])
+                added_pred = pred - pred0
+                row = {"n": n, "placement": label, "added_predicted_us": added_pred, "added_measured_us": added_meas,
+                       "added_error_pct": 100.0 * abs(added_meas - added_pred) / max(abs(added_meas), 1e-9)}
+                # the pass launches alone: their own predicted and measured times
+                for name, b, f in r["rep"]["kernels"]:
+                    if name in ("oft_pass", "s_pass"):
+                        p_us = b / (hbm * 1e3) + launch_us
+                        m_us = 1e3 * r["kernel_ms"].get(name, float("nan"))
+                        row[name] = {"bytes": b, "predicted_us": p_us, "measured_us": m_us,
+                                     "error_pct": 100.0 * abs(m_us - p_us) / m_us}
+                rows.append(row)
+        ctx.set_variant(0)
+        if ctx.sync_status() != 0:
+            raise RuntimeError("device status error in the validation leg")
+    finally:
+        ctx.close()
+    pass_err = [r[k]["error_pct"] for r in rows for k in ("oft_pass", "s_pass") if k in r]
+    added_err = [r["added_error_pct"] for r in rows]
+    return {"workload": "decode_mixed projections q,k,v,gate,up,down at 16/32/64/128 tokens; placements of the "
+                        "rotation and of DoRA's and (IA)^3's s in launches of their own",
+            "hbm_gbs": hbm, "peak_kind": peak_kind, "launch_us": launch_us, "rows": rows,
+            "median_error_pct_pass_launches": float(np.median(pass_err)) if pass_err else None,
+            "median_error_pct_added_time": float(np.median(added_err)) if added_err else None}
+
+
 # ------------------------------------------------------------------ GPU arm
 def main():
     args = parse()
@@ -815,7 +896,8 @@ def main():
     torch.cuda.empty_cache()
     if rank == 0 and world == 1:
         for key, skip, fn in (("prefill", args.no_prefill, prefill_leg), ("scaling", args.no_scaling, scaling_leg),
-                              ("stack", args.no_stack, stack_leg)):
+                              ("stack", args.no_stack, stack_leg),
+                              ("time_model_validation", args.no_validation, validation_leg)):
             if skip:
                 continue
             try:

@@ -302,7 +302,10 @@ scute_status scute_index_tokens_noalloc(const int8_t *method_of_adapter, int32_t
  * each distinct adapter's live (post-fold) tensors once, the shared VeRA pair
  * once when a VeRA token is present, x read, out written and the ids read.
  * Launch plans: a bf16 batch of at most 128 tokens is ONE launch ("step") over
- * every layer of the call; otherwise each layer takes the per-kernel plan
+ * every layer of the call, with "oft_pass" before it and "s_pass" after it
+ * when the variant flags place those slots in passes of their own
+ * (scute_set_variant; the step's own bytes then lose R, or the DoRA and
+ * (IA)^3 s vectors); otherwise each layer takes the per-kernel plan
  * ("index", "rotate", "base_gemm", "lr_shrink", "lr_expand", "vera_shrink",
  * "vera_expand").  Pure host arithmetic: no device work, no context needed for
  * scute_byte_model and scute_byte_model_batch. */
@@ -335,6 +338,7 @@ typedef struct {
     int vera_launched;        /* the per-kernel plan launches the VeRA kernels */
     int max_adapters;
     const scute_bm_adapter *adapters;  /* [max_adapters]                       */
+    int variant;              /* SCUTE_VARIANT_* flags of the call (0: none)   */
 } scute_bm_layer;
 
 /* One call of one layer (scute_linear). */
@@ -390,7 +394,9 @@ enum {
     SCUTE_KIND_BASE_GEMM = 3,    /* base GEMM with the s / b epilogue          */
     SCUTE_KIND_LOWRANK = 4,      /* owned low-rank shrink and expand (2 launches) */
     SCUTE_KIND_VERA_SHRINK = 5,  /* VeRA shared shrink GEMM                    */
-    SCUTE_KIND_VERA_EXPAND = 6   /* VeRA shared expand GEMM                    */
+    SCUTE_KIND_VERA_EXPAND = 6,  /* VeRA shared expand GEMM                    */
+    SCUTE_KIND_OFT_PASS = 7,     /* rotation as its own pass (scute_set_variant) */
+    SCUTE_KIND_S_PASS = 8        /* s as its own pass (scute_set_variant)      */
 };
 scute_status scute_timing_enable(scute_ctx *ctx, int enable);
 scute_status scute_timing_reset(scute_ctx *ctx);
@@ -405,6 +411,28 @@ scute_status scute_timing_kinds(const scute_ctx *ctx, int *kinds_out, int max, i
  * the hook applies to that one launch only.  Nothing traps or faults. */
 #define SCUTE_INJECT_STALL 1
 scute_status scute_debug_inject(scute_ctx *ctx, int what);
+
+/* Separate-pass placements of two live slots, for validating the byte and
+ * time model (article, section "Where is the cheapest place to compute the
+ * remaining slots?": the model is checked there on OFT's input rotation and
+ * on applying DoRA's s outside the expand).  With flags = 0 (the default) the
+ * decode step applies every slot inside its one launch.  Otherwise a bf16
+ * decode batch (n <= 128) of this context adds, around its step launch:
+ *   SCUTE_VARIANT_OFT_PASS  one launch before the step that writes x R for
+ *                           the rotated tokens (x for the others) into a
+ *                           context-owned copy, which the step then reads;
+ *   SCUTE_VARIANT_S_PASS    one launch after the step that multiplies the
+ *                           output rows of DoRA and (IA)^3 tokens by their s,
+ *                           which the step then leaves out (DoRA expanding
+ *                           with B' whose s is not folded in).
+ * Results stay those of the normal form up to rounding order.  Other batches
+ * (fp32 contexts, more than 128 tokens) ignore the flags.  A setup call:
+ * SCUTE_VARIANT_OFT_PASS allocates the rotated-copy workspace here, so do not
+ * make it during stream capture.  scute_predict_batch describes the launches
+ * of the flags in force. */
+#define SCUTE_VARIANT_OFT_PASS 1
+#define SCUTE_VARIANT_S_PASS 2
+scute_status scute_set_variant(scute_ctx *ctx, int flags);
 
 /* Test hook for the out-of-memory path (no counterpart in the article).  The
  * k-th device allocation the library makes after this call (counted over

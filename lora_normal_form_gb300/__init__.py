@@ -66,7 +66,7 @@ class BmLayer(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("out_dtype", ctypes.c_int), ("d_in", ctypes.c_int),
                 ("d_out", ctypes.c_int), ("shared_rank", ctypes.c_int),
                 ("lowrank_launched", ctypes.c_int), ("vera_launched", ctypes.c_int),
-                ("max_adapters", ctypes.c_int), ("adapters", ctypes.POINTER(BmAdapter))]
+                ("max_adapters", ctypes.c_int), ("adapters", ctypes.POINTER(BmAdapter)), ("variant", ctypes.c_int)]
 
 
 class Call(ctypes.Structure):
@@ -119,6 +119,7 @@ _SIGS = {
     "scute_timing_reset": (ctypes.c_int, [ctypes.c_void_p]),
     "scute_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_debug_fail_alloc": (None, [ctypes.c_int]),
+    "scute_set_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]),
     "scute_timing_kinds": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -355,6 +356,15 @@ def scute_debug_inject(ctx, what: int) -> None:
     _check(ctx, load().scute_debug_inject(ctx, what))
 
 
+VARIANT_OFT_PASS, VARIANT_S_PASS = 1, 2
+
+
+def scute_set_variant(ctx, flags: int) -> None:
+    """Place OFT's rotation (1) and / or DoRA's and (IA)^3's s (2) in launches
+    of their own around the decode step (byte-model validation)."""
+    _check(ctx, load().scute_set_variant(ctx, int(flags)))
+
+
 def scute_debug_fail_alloc(k: int) -> None:
     """Make the k-th device allocation of the library from now fail as out of
     memory (test hook; k <= 0 switches it off)."""
@@ -368,7 +378,7 @@ def scute_timing_read(ctx, max_slots: int = TIMING_SLOTS) -> list:
     return [float(buf[i]) for i in range(n.value)]
 
 
-KIND_NAMES = ("step", "index", "rotate", "base_gemm", "lowrank", "vera_shrink", "vera_expand")
+KIND_NAMES = ("step", "index", "rotate", "base_gemm", "lowrank", "vera_shrink", "vera_expand", "oft_pass", "s_pass")
 
 
 def scute_timing_kinds(ctx, max_slots: int = TIMING_SLOTS) -> list:

@@ -6,7 +6,8 @@ import numpy as np
 from . import (BF16, FP32, METHOD_ID, scute_add_layer, scute_create, scute_debug_index, scute_destroy,
                scute_launch_count, scute_linear, scute_linear_batch, scute_linear_batch_host,
                scute_linear_host, scute_predict_batch, scute_predict_bytes,
-               scute_register_adapter, scute_set_shared, scute_sync_status, scute_timing_enable,
+               scute_register_adapter, scute_set_shared, scute_set_variant, scute_sync_status,
+               scute_timing_enable,
                scute_timing_kinds, scute_timing_read, scute_timing_reset, scute_unregister_adapter)
 
 
@@ -115,6 +116,9 @@ class Context:
         ids_host = np.ascontiguousarray(ids_host, dtype=np.int32)
         return scute_predict_batch(self.handle, list(layers), ids_host, int(ids_host.size),
                                    BF16 if out_dtype == "bf16" else FP32)
+
+    def set_variant(self, flags: int):
+        scute_set_variant(self.handle, flags)
 
     def launch_count(self) -> int:
         return scute_launch_count(self.handle)

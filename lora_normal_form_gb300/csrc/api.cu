@@ -244,7 +244,7 @@ void scute_destroy(scute_ctx *c) {
     void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
                     c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_v, c->step_part,
-                    c->step_sync, c->step_hx, c->step_hout};
+                    c->step_sync, c->step_hx, c->step_hout, c->var_x};
     for (void *p : bufs)
         if (p) cudaFree(p);
     if (c->ev_made)
@@ -296,6 +296,7 @@ scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const
         st = grow(c, &c->step_xs, &c->step_xs_cols, (size_t)L.kdim, c->esz, rows);
         if (!st) st = grow(c, &c->step_hx, &c->step_hx_cols, (size_t)d_in, c->esz, rows);
         if (!st) st = grow(c, &c->step_hout, &c->step_hout_cols, (size_t)d_out, 4, rows);
+        if (!st && (c->variant & VARIANT_OFT_PASS)) st = grow(c, &c->var_x, &c->var_x_cols, (size_t)d_in, c->esz, rows);
         int max_ft = 0;
         for (const auto &Lr : c->layers)
             if (Lr.present && (Lr.d_out + 127) / 128 > max_ft) max_ft = (Lr.d_out + 127) / 128;
@@ -433,6 +434,8 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
         if (al.R) total += align256((size_t)L.d_in * OFT_BLK * E) * (c->dtype == SCUTE_BF16 ? 2 : 1);
         if (al.rank) {
             total += align256((size_t)al.rank * L.d_in * E) + align256((size_t)al.rank * L.d_out * E);
+            // DoRA also keeps B' without its s (read only by the separate-s-pass placement)
+            if (method == SCUTE_DORA) total += align256((size_t)al.rank * L.d_out * E);
             size_t need = align256((size_t)L.d_in * al.rank * E) + align256((size_t)al.rank * L.d_out * E) +
                           3 * align256(4 * (size_t)L.d_out) + align256(4 * (size_t)al.rank);
             if (need > tmp_need) tmp_need = need;
@@ -503,6 +506,11 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
             }
             REG_TRY(launch_fold_A(f32, tA, L.d_in, al.rank, x.c, dvec, Ap, 0));
             REG_TRY(launch_fold_B(f32, tB, al.rank, L.d_out, evec, svec, Bp, 0));
+            if (method == SCUTE_DORA) {
+                void *Bu = take((size_t)al.rank * L.d_out * E);
+                REG_TRY(launch_fold_B(f32, tB, al.rank, L.d_out, nullptr, nullptr, Bu, 0));
+                s.Bu = Bu;
+            }
             s.A = Ap;
             s.B = Bp;
             s.rank = al.rank;
@@ -622,13 +630,26 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
     const int G = c->num_sms < STEP_MAX_GRID ? c->num_sms : STEP_MAX_GRID;
     const int BN = nn <= 64 ? 64 : 128;
     if (BN > c->step_bn_max) return fail(c, SCUTE_ERR_UNSUPPORTED, "decode workspace sized for fewer tokens");
+    const bool oft_pass = (c->variant & VARIANT_OFT_PASS) != 0, s_pass = (c->variant & VARIANT_S_PASS) != 0;
+    int max_din = 0, max_dout = 0;
+    for (int i = 0; i < nc; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        if (L.d_in > max_din) max_din = L.d_in;
+        if (L.d_out > max_dout) max_dout = L.d_out;
+    }
+    if (oft_pass && (size_t)max_din > c->var_x_cols)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "rotated-copy workspace smaller than a layer's input");
     long long blk = 0;
     int tile = 0, item = 0, rmax = 0;
     for (int i = 0; i < nc; ++i) {
         const LayerRec &L = c->layers[calls[i].layer];
         StepCall &k = a.call[i];
         const bool vera_on = L.rv > 0 && L.n_vera > 0;
-        k.x = calls[i].x;
+        // the rotation placed in a separate pass: the token operand is read
+        // from that pass's rotated copy of x
+        k.x = oft_pass ? reinterpret_cast<uint8_t *>(c->var_x) + (size_t)i * STEP_MAX_TOKENS * c->var_x_cols * c->esz
+                       : calls[i].x;
+        k.x0 = calls[i].x;
         k.xs = reinterpret_cast<uint8_t *>(c->step_xs) + (size_t)i * STEP_MAX_TOKENS * c->step_xs_cols * c->esz;
         k.U = vera_on ? reinterpret_cast<uint8_t *>(c->step_U) + (size_t)i * STEP_MAX_TOKENS * c->step_u_cols * c->esz
                       : nullptr;
@@ -738,12 +759,42 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
     if ((size_t)(units + tile + G) * 2 * 128 * BN > c->step_part_floats)
         return fail(c, SCUTE_ERR_UNSUPPORTED, "partial-tile workspace too small for this batch");
     if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
+    a.variant = c->variant;
+    PassArgs pa;
+    memset(&pa, 0, sizeof(pa));
+    pa.n_calls = nc;
+    pa.n = nn;
+    pa.A = c->max_adapters;
+    pa.out_f32 = out_f32;
+    pa.ids = ids;
+    pa.method_tab = c->d_method;
+    for (int i = 0; i < nc; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        pa.call[i].x = calls[i].x;
+        pa.call[i].xo = const_cast<void *>(a.call[i].x);
+        pa.call[i].out = calls[i].out;
+        pa.call[i].slots = a.call[i].slots;
+        pa.call[i].d_in = L.d_in;
+        pa.call[i].d_out = L.d_out;
+    }
     TimedLaunch tl{c, st};
-    CU_TRY(c, tl.begin());
     cudaGetLastError();
+    if (oft_pass) {
+        CU_TRY(c, tl.begin());
+        CU_TRY(c, launch_oft_pass(pa, max_din, st));
+        CU_TRY(c, tl.end(SCUTE_KIND_OFT_PASS));
+        count_launch(c, 1);
+    }
+    CU_TRY(c, tl.begin());
     CU_TRY(c, launch_step(a, st));
     CU_TRY(c, tl.end(SCUTE_KIND_STEP));
     count_launch(c, 1);
+    if (s_pass) {
+        CU_TRY(c, tl.begin());
+        CU_TRY(c, launch_s_pass(pa, max_dout, st));
+        CU_TRY(c, tl.end(SCUTE_KIND_S_PASS));
+        count_launch(c, 1);
+    }
     return SCUTE_OK;
 }
 
@@ -1052,6 +1103,22 @@ scute_status scute_timing_reset(scute_ctx *c) {
 }
 
 void scute_debug_fail_alloc(int k) { g_fail_alloc.store(k > 0 ? k : 0); }
+
+scute_status scute_set_variant(scute_ctx *c, int flags) {
+    if (!c) return SCUTE_ERR_ARG;
+    if (flags & ~(SCUTE_VARIANT_OFT_PASS | SCUTE_VARIANT_S_PASS)) return fail(c, SCUTE_ERR_ARG, "unknown variant %d", flags);
+    if ((flags & SCUTE_VARIANT_OFT_PASS) && c->dtype == SCUTE_BF16) {
+        DeviceGuard dg(c->device);
+        size_t need = 0;
+        for (const auto &L : c->layers)
+            if (L.present && (size_t)L.d_in > need) need = (size_t)L.d_in;
+        const scute_status st = grow(c, &c->var_x, &c->var_x_cols, need, c->esz,
+                                     (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS);
+        if (st) return st;
+    }
+    c->variant = flags;
+    return SCUTE_OK;
+}
 
 scute_status scute_debug_inject(scute_ctx *c, int what) {
     if (!c) return SCUTE_ERR_ARG;

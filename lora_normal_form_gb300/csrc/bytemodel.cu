@@ -30,6 +30,7 @@ struct LayerCount {
     int64_t E, Eo, din, dout, kd, rv, krv, n;
     int64_t distinct = 0, n_lr = 0, lr_rank_rows = 0, n_v = 0, n_rot = 0, segs = 0;
     int64_t live = 0, R = 0, sb = 0, A = 0, B = 0, d = 0, e = 0;
+    int64_t n_s = 0, s_pass_vec = 0;   // DoRA / (IA)^3 tokens with a live s, and their distinct s bytes
     int64_t W() const { return din * dout * E; }
     int64_t shared() const { return n_v > 0 ? (din + dout) * rv * E : 0; }
     int64_t x() const { return n * din * E; }
@@ -71,7 +72,10 @@ bool count_layer(const scute_bm_layer *L, const int32_t *ids, int64_t n, LayerCo
         }
         if (ad.has_vera) ++c.n_v;
         if (ad.has_R) ++c.n_rot;
+        const bool sp = ad.has_s && (ad.method == SCUTE_DORA || ad.method == SCUTE_IA3);
+        if (sp) ++c.n_s;
         if (seen[a]) continue;
+        if (sp) c.s_pass_vec += 4 * c.dout;
         seen[a] = 1;
         ++c.distinct;
         if (ad.has_s) { c.live += 4 * c.dout; c.sb += 4 * c.dout; }
@@ -149,9 +153,33 @@ scute_status scute_byte_model_batch(const scute_bm_layer *layers, int n_layers, 
         wbytes += c.W();
     }
     if (step) {
-        int64_t fl = 0;
+        const int var = layers[0].variant;
+        int64_t fl = 0, step_bytes = alg;
         for (const LayerCount &c : cs) fl += c.flops();
-        add_kernel(rep, "step", alg, fl);
+        if (var & SCUTE_VARIANT_OFT_PASS) {
+            // x read, R of each distinct rotating adapter, the rotated copy
+            // written (per layer), ids once; the step no longer reads R
+            int64_t b = 4 * n, f = 0;
+            for (const LayerCount &c : cs) {
+                b += 2 * c.n * c.din * c.E + c.R;
+                f += 2 * c.n_rot * c.din * 32;
+                step_bytes -= c.R;
+            }
+            fl -= f;
+            add_kernel(rep, "oft_pass", b, f);
+        }
+        int64_t sb = 4 * n, sf = 0;
+        if (var & SCUTE_VARIANT_S_PASS) {
+            // the DoRA and (IA)^3 rows of out read and written again, their
+            // distinct s vectors, ids once; the step no longer reads those s
+            for (const LayerCount &c : cs) {
+                sb += 2 * c.n_s * c.dout * c.Eo + c.s_pass_vec;
+                sf += c.n_s * c.dout;
+                step_bytes -= c.s_pass_vec;
+            }
+        }
+        add_kernel(rep, "step", step_bytes, fl);
+        if (var & SCUTE_VARIANT_S_PASS) add_kernel(rep, "s_pass", sb, sf);
     } else {
         for (int i = 0; i < n_layers; ++i) {
             if (rep->n_kernels + 7 > SCUTE_BM_MAX_KERNELS) return SCUTE_ERR_UNSUPPORTED;
@@ -208,6 +236,7 @@ static void fill_layer(const scute_ctx *c, int layer, scute_dtype out_dtype, std
     bl.vera_launched = L.rv > 0 && L.n_vera > 0;
     bl.max_adapters = c->max_adapters;
     bl.adapters = ads.data();
+    bl.variant = c->variant;
 }
 
 scute_status scute_predict_bytes(const scute_ctx *c, const int32_t *ids, int64_t n, int layer,

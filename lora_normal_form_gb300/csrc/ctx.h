@@ -91,6 +91,9 @@ struct scute_ctx {
     int step_bn_max = 64;
     int smem_optin = 0;
     int inject = 0;              // scute_debug_inject, consumed by the next decode launch
+    int variant = 0;             // scute_set_variant: slots placed in separate passes
+    void *var_x = nullptr;       // rotated copies of the calls' x (separate rotation pass)
+    size_t var_x_cols = 0;
     PFN_encodeTiled encode = nullptr;
     int64_t launches = 0;
     bool timing = false;

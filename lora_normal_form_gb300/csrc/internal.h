@@ -35,9 +35,14 @@ struct Slot {
     const float *vd;   // VeRA d [shared rank] (c folded in); null = no shared term
     const float *ve;   // VeRA e [d_out]; null = ones
     const void *Rt;    // R with every 32x32 block transposed (bf16 contexts; null = no R)
+    const void *Bu;    // DoRA: B' without its s folded in (the separate-s-pass placement)
     int rank;          // rank of the owned term (0 = none)
     int pad;
 };
+
+// Separate-pass placements of live slots (scute_set_variant; the same codes as
+// SCUTE_VARIANT_OFT_PASS and SCUTE_VARIANT_S_PASS).
+enum : int { VARIANT_OFT_PASS = 1, VARIANT_S_PASS = 2 };
 
 // Results of the token indexing kernel beyond the per-row arrays.
 struct IndexMeta {
@@ -183,7 +188,8 @@ struct StepCall {
     CUtensorMap mapBsh;        // B_sh^T [d_out][krv]
     CUtensorMap mapU;          // VeRA intermediate [128][krv]
     CUtensorMap mapX;          // caller input [n][d_in] (VeRA shrink operand when vs_x)
-    const void *x;             // [n][d_in] caller input
+    const void *x;             // [n][d_in] token-operand source (the caller's x, or its rotated copy)
+    const void *x0;            // [n][d_in] the caller's x (low-rank shrink input)
     void *xs;                  // [128][kdim]
     void *U;                   // [128][krv]
     float *v;                  // [128][MAX_RANK]
@@ -222,11 +228,29 @@ struct StepArgs {
     int n_items;               // prologue items over all calls
     int rmax;                  // largest lr_rmax (shared-memory v rows)
     int hold;                  // extra count the token-operand wait needs (failure-path test)
+    int variant;               // VARIANT_*: slots applied by separate passes instead
     long long start[STEP_MAX_GRID + 1];   // main-block range of each CTA: [start[i], start[i+1])
 };
 
 size_t step_smem_bytes(int bn, int stages, int rmax);
 cudaError_t launch_step(const StepArgs &a, cudaStream_t st);
+
+// ---------------------------------------------------------------- separate passes
+struct PassCall {
+    const void *x;     // oft_pass: input [n][d_in]
+    void *xo;          // oft_pass: rotated copy [n][d_in]
+    void *out;         // s_pass: output [n][d_out], scaled in place
+    const Slot *slots;
+    int d_in, d_out;
+};
+struct PassArgs {
+    PassCall call[STEP_MAX_CALLS];
+    int n_calls, n, A, out_f32;
+    const int32_t *ids;
+    const int8_t *method_tab;
+};
+cudaError_t launch_oft_pass(const PassArgs &p, int max_d_in, cudaStream_t st);
+cudaError_t launch_s_pass(const PassArgs &p, int max_d_out, cudaStream_t st);
 
 // ---------------------------------------------------------------- other kernels
 // Token indexing (one CTA).  seg_unit (optional, n_seg + 1 ints): the

@@ -14,6 +14,7 @@
 // parts [hi | hi | lo] for the split-precision GEMM (hi = tf32(v), lo = v - hi).
 // bf16 contexts: gather_rotate_bf16_kernel below.
 #include "internal.h"
+#include "oft_lane.cuh"
 #include "ptx.cuh"
 
 namespace scute {
@@ -83,12 +84,10 @@ __global__ void __launch_bounds__(256) gather_rotate_kernel(const T *__restrict_
 }
 
 // bf16 contexts: one warp per sorted row and 256-column chunk, lane l moving
-// columns [8l, 8l + 8) with one 16-byte load and store.  A rotated row's lane
-// computes its 8 outputs of one 32x32 block: the block's 32 inputs come from
-// the block's 4 lanes by shuffle, and output column j reads row j of the
-// block-transposed copy of R (32 contiguous bf16) through L1, where the rows of
-// one adapter that the same CTA handles find it again.  No shared memory and
-// no barrier: every row is independent.
+// columns [8l, 8l + 8) with one 16-byte load and store; a rotated row's lanes
+// compute their block outputs with rotate_lane (oft_lane.cuh), reading R
+// through L1, where the rows of one adapter that the same CTA handles find it
+// again.  No shared memory and no barrier: every row is independent.
 __global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int d_in,
                                                                  int n, const int *__restrict__ perm,
                                                                  const int *__restrict__ aid_s,
@@ -117,47 +116,7 @@ __global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bflo
         const __nv_bfloat16 *Rt =
             ad[r] >= 0 ? reinterpret_cast<const __nv_bfloat16 *>(slots[ad[r]].Rt) : nullptr;
         uint4 o = xv[r];
-        if (Rt != nullptr) {
-            // the 32 inputs of this lane's block, as 16 bf16 pairs
-            uint32_t xin[16];
-            const uint32_t *mine = reinterpret_cast<const uint32_t *>(&xv[r]);
-            const int base = lane & ~3;
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-                for (int w = 0; w < 4; ++w) xin[s4 * 4 + w] = __shfl_sync(0xffffffffu, mine[w], base + s4);
-            float xf[32];
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xin[p]));
-                xf[2 * p] = f.x;
-                xf[2 * p + 1] = f.y;
-            }
-            if (colok) {
-                const int b = col / OFT_BLK, j0 = col % OFT_BLK;
-                const uint4 *Rrow = reinterpret_cast<const uint4 *>(Rt + ((size_t)b * OFT_BLK + j0) * OFT_BLK);
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 u = __ldg(Rrow + e * 4 + q);
-                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const float2 f = __bfloat1622float2(h[t]);
-                            acc = fmaf(xf[q * 8 + 2 * t], f.x, acc);
-                            acc = fmaf(xf[q * 8 + 2 * t + 1], f.y, acc);
-                        }
-                    }
-                    y[e] = acc;
-                }
-                __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) h[t] = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);
-            }
-        }
+        if (Rt != nullptr) o = rotate_lane(xv[r], Rt, col, colok);
         if (colok) *reinterpret_cast<uint4 *>(xs + (size_t)i * kdim + col) = o;
     }
 }

@@ -309,10 +309,14 @@ __device__ void stage_meta(const StepArgs &a, int c, Fixed &fx, Ctrl *ctrl, int 
         const int aid = fx.tok_aid[t];
         if (aid >= 0) {
             const Slot &sl = k.slots[aid];
-            m.s = sl.s;
+            // s placed in a separate pass: DoRA and (IA)^3 tokens leave it out
+            // here, and DoRA expands with B' whose s is not folded in
+            const int meth = a.method_tab[aid];
+            const bool spass = (a.variant & VARIANT_S_PASS) && (meth == RANK_DORA || meth == RANK_IA3);
+            m.s = spass ? nullptr : sl.s;
             m.b = sl.b;
             if (k.lr_rmax > 0 && sl.B && sl.rank > 0) {
-                m.B = reinterpret_cast<const __nv_bfloat16 *>(sl.B);
+                m.B = reinterpret_cast<const __nv_bfloat16 *>(spass && sl.Bu ? sl.Bu : sl.B);
                 m.rank = sl.rank;
             }
             m.vd = sl.vd;
@@ -804,7 +808,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 if (aid >= 0) {
                     const StepCall &k = a.call[c];
                     const Slot &sl = k.slots[aid];
-                    R[r] = reinterpret_cast<const __nv_bfloat16 *>(sl.Rt);
+                    // rotation placed in a separate pass: x is already rotated
+                    R[r] = (a.variant & VARIANT_OFT_PASS) ? nullptr : reinterpret_cast<const __nv_bfloat16 *>(sl.Rt);
                     if (sl.A && sl.rank > 0 && k.lr_rmax > 0) {
                         Ao[r] = reinterpret_cast<const __nv_bfloat16 *>(sl.A);
                         rk[r] = sl.rank;
@@ -1064,7 +1069,9 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             }
             if (kk < 0) continue;   // uniform across the CTA
             const StepCall &k = a.call[c];
-            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
+            // the low-rank term acts on x, not on x R (x0: the caller's x even
+            // when the token operand comes from a separately rotated copy)
+            const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x0);
             {
                 // owned low-rank shrink: LR_Q ranks of one segment
                 const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;

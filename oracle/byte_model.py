@@ -52,6 +52,10 @@ def _layer_counts(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, 
             n_rot += 1
         if a not in seen:
             seen.append(a)
+    # tokens of DoRA / (IA)^3 adapters with a live s, and those adapters' distinct s bytes
+    n_s = sum(1 for a in ids if int(a) in adapters and adapters[int(a)]["s"]
+              and adapters[int(a)]["method"] in ("dora", "ia3"))
+    s_pass_vec = 4 * d_out * sum(1 for a in seen if adapters[a]["s"] and adapters[a]["method"] in ("dora", "ia3"))
     live = R_b = sb_b = A_b = B_b = d_b = e_b = 0
     for a in seen:
         ad = adapters[a]
@@ -74,6 +78,7 @@ def _layer_counts(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, 
             if ad["vera_e"]:
                 live += 4 * d_out
                 e_b += 4 * d_out
+    c.update(n_s=n_s, s_pass_vec=s_pass_vec)
     c.update(seen=seen, segments=len(seen) + (1 if has_base else 0), n_lr=n_lr, lr_rank_rows=lr_rank_rows,
              n_v=n_v, n_rot=n_rot, live=live, R_b=R_b, sb_b=sb_b, A_b=A_b, B_b=B_b, d_b=d_b, e_b=e_b)
     c["shared"] = (d_in + d_out) * shared_rank * E if n_v else 0
@@ -117,7 +122,7 @@ def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool) -> list:
     return kernels
 
 
-def batch_bytes(ids, layers: list, dtype: str, out_dtype: str) -> dict:
+def batch_bytes(ids, layers: list, dtype: str, out_dtype: str, variant: int = 0) -> dict:
     """Launch list and algorithmic bytes of one batched call over ``layers``
     (each a dict with keys adapters, d_in, d_out, shared_rank,
     lowrank_launched, vera_launched) that read the same ids.
@@ -131,7 +136,22 @@ def batch_bytes(ids, layers: list, dtype: str, out_dtype: str) -> dict:
           for L in layers]
     alg = 4 * n + sum(c["alg_no_ids"] for c in cs)
     if dtype != "fp32" and n <= 128:
-        kernels = [("step", alg, sum(c["flops"] for c in cs))]
+        # separate-pass placements (variant bits 1: rotation, 2: DoRA / (IA)^3 s)
+        step_bytes, step_flops = alg, sum(c["flops"] for c in cs)
+        kernels = []
+        if variant & 1:
+            b = 4 * n + sum(2 * c["n"] * c["d_in"] * c["E"] + c["R_b"] for c in cs)
+            f = sum(2 * c["n_rot"] * c["d_in"] * 32 for c in cs)
+            step_bytes -= sum(c["R_b"] for c in cs)
+            step_flops -= f
+            kernels.append(("oft_pass", b, f))
+        if variant & 2:
+            sb = 4 * n + sum(2 * c["n_s"] * c["d_out"] * c["Eo"] + c["s_pass_vec"] for c in cs)
+            sf = sum(c["n_s"] * c["d_out"] for c in cs)
+            step_bytes -= sum(c["s_pass_vec"] for c in cs)
+        kernels.append(("step", step_bytes, step_flops))
+        if variant & 2:
+            kernels.append(("s_pass", sb, sf))
     else:
         kernels = []
         for L, c in zip(layers, cs):

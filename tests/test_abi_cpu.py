@@ -212,3 +212,63 @@ def test_time_model_hand_example(lib):
     assert abs(OBM.predict_time_us(rep["kernels"], 1000.0, 0.0, 0.5) - 5.0) <= 1e-12
     with pytest.raises(lib.ScuteError):
         lib.scute_predict_time(rep, 0.0, 0.0, 0.5)
+
+
+def _bm_layer_struct(lib, ads, dtype, out_dtype, d_in, d_out, shared_rank, lowrank, vera, A, variant, keep):
+    import ctypes
+    arr = (lib.BmAdapter * A)()
+    for i in range(A):
+        arr[i].method = -1
+    for aid, v in ads.items():
+        arr[aid].method = lib.METHOD_ID[v["method"]]
+        arr[aid].rank = v["rank"]
+        arr[aid].has_s, arr[aid].has_b, arr[aid].has_R = int(v["s"]), int(v["b"]), int(v["R"])
+        arr[aid].has_vera, arr[aid].has_vera_e = int(v["vera"]), int(v["vera_e"])
+    keep.append(arr)
+    return lib.BmLayer(dtype=lib.FP32 if dtype == "fp32" else lib.BF16,
+                       out_dtype=lib.FP32 if out_dtype == "fp32" else lib.BF16, d_in=d_in, d_out=d_out,
+                       shared_rank=shared_rank, lowrank_launched=int(lowrank), vera_launched=int(vera),
+                       max_adapters=A, adapters=ctypes.cast(arr, ctypes.POINTER(lib.BmAdapter)), variant=variant)
+
+
+def test_variant_byte_model_hand_example(lib):
+    """The separate-pass placements counted by hand (tests/golden/byte_model_hand.json)."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "byte_model_hand.json")))
+    for c in g["variant_cases"]:
+        ads = {int(k): v for k, v in c["adapters"].items()}
+        L = {"adapters": ads, "d_in": c["d_in"], "d_out": c["d_out"], "shared_rank": c["shared_rank"],
+             "lowrank_launched": c["lowrank_launched"], "vera_launched": c["vera_launched"]}
+        ref = OBM.batch_bytes(c["ids"], [L], c["dtype"], c["out_dtype"], c["variant"])
+        exp = c["expected"]
+        assert [list(k) for k in ref["kernels"]] == exp["kernels"]
+        assert ref["algorithmic_bytes"] == exp["algorithmic_bytes"]
+        assert ref["adapter_bytes"] == exp["adapter_bytes"]
+        keep = []
+        bl = _bm_layer_struct(lib, ads, c["dtype"], c["out_dtype"], c["d_in"], c["d_out"], c["shared_rank"],
+                              c["lowrank_launched"], c["vera_launched"], 8, c["variant"], keep)
+        got = lib.scute_byte_model_batch([bl], np.array(c["ids"], np.int32), len(c["ids"]))
+        assert [list(k) for k in got["kernels"]] == exp["kernels"]
+        assert got["algorithmic_bytes"] == exp["algorithmic_bytes"]
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_variant_byte_model_matches_oracle(lib, variant):
+    """The decode workload's six projections with each placement: the
+    library's launch list equals the oracle's, and the per-launch bytes add up
+    to the algorithmic bytes plus what the passes move again."""
+    w = WL.decode_mixed()
+    names = ("q", "k", "v", "gate", "up", "down")
+    A = max(a.id for a in w.adapters) + 3
+    keep, layers, ref_layers = [], [], []
+    for name in names:
+        L, ads, lowrank, vera = _bm_inputs(w, name, "bf16")
+        layers.append(_bm_layer_struct(lib, ads, "bf16", "bf16", L.d_in, L.d_out, L.shared_rank, lowrank, vera, A,
+                                       variant, keep))
+        ref_layers.append({"adapters": ads, "d_in": L.d_in, "d_out": L.d_out, "shared_rank": L.shared_rank,
+                           "lowrank_launched": lowrank, "vera_launched": vera})
+    ids = np.ascontiguousarray(w.ids, np.int32)
+    got = lib.scute_byte_model_batch(layers, ids, int(ids.size))
+    ref = OBM.batch_bytes(ids, ref_layers, "bf16", "bf16", variant)
+    assert got["kernels"] == [tuple(k) for k in ref["kernels"]]
+    names_got = [k[0] for k in got["kernels"]]
+    assert names_got == (["oft_pass"] if variant & 1 else []) + ["step"] + (["s_pass"] if variant & 2 else [])

@@ -146,6 +146,26 @@ def test_small_decode_batch_parity(scute, out_dtype, n):
     ctx.close()
 
 
+@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_separate_pass_variants(scute, variant, out_dtype):
+    """The rotation (1) and DoRA's / (IA)^3's s (2) placed in launches of their
+    own around the decode step: one extra launch each, results still the
+    oracle's (the raw normal-form adapter with R and an owned term checks that
+    the low-rank shrink keeps reading x, not the rotated copy)."""
+    w = _small_decode(50)
+    ctx = H.make_ctx(scute, w)
+    ctx.set_variant(variant)
+    names = list(SMALL_NAMES)
+    n0 = ctx.launch_count()
+    outs = _batch_run(ctx, w, names, out_dtype)
+    assert ctx.launch_count() - n0 == 1 + (variant & 1) + (variant >> 1)
+    assert ctx.sync_status() == 0
+    for name, o in zip(names, outs):
+        H.grade(w, name, o, out_dtype)
+    ctx.close()
+
+
 def test_batch_repeats_bit_for_bit(scute):
     """Partial tiles are summed in a fixed order, whichever CTA finishes a tile,
     so repeated calls give identical bits."""
