@@ -428,6 +428,10 @@ def prefill_leg(scute, dev, flush, launch_us, steps=6):
                              frac=f / (t * 1e-3) / 1e12 / attainable, bound="tensor" if attainable >= tf_peak else "hbm")
                 else:
                     e.update(frac=e["gbs"] / hbm, bound="hbm")
+                # the time model for this launch (the low-rank pair is two launches)
+                nl = 2 if k == "lowrank" else 1
+                e["predicted_us"] = max(b / (hbm * 1e3), f / (tf_peak * 1e6)) + nl * launch_us
+                e["model_error_pct"] = 100.0 * abs(1e3 * t - e["predicted_us"]) / (1e3 * t)
                 kern[k] = e
             g = kern["base_gemm"]["ms"]
             pure, full = predicted(scute, rep, hbm, tf_peak, launch_us)

@@ -71,7 +71,7 @@ __device__ __forceinline__ bool unit_rows(int u, const int *__restrict__ seg_sta
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256, 2) lr_shrink_kernel(const T *__restrict__ x, int d_in,
+__global__ void __launch_bounds__(256, 3) lr_shrink_kernel(const T *__restrict__ x, int d_in,
                                                            const int *__restrict__ perm,
                                                            const int *__restrict__ seg_start,
                                                            const int *__restrict__ seg_aid,
