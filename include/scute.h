@@ -443,6 +443,27 @@ scute_status scute_set_variant(scute_ctx *ctx, int flags);
  * device work is involved. */
 void scute_debug_fail_alloc(int k);
 
+/* The plan of the context's last decode-step launch (the host values that
+ * launch was given), so that the kernel's index arithmetic can be checked
+ * against its buffers on the host.  The article has no counterpart.  Writes at
+ * most `cap` int64 values to the HOST array `out`:
+ *   SCUTE_PLAN_HEAD values: n_calls, n, bn (tokens per tile), stages, grid,
+ *     n_units (VeRA shrink units), vs_ch (K blocks per unit), n_tiles,
+ *     n_items (low-rank shrink items), rmax, t_main (main K blocks), hold,
+ *     smem_bytes (before the one-CTA-per-SM floor), smem_optin,
+ *     part_floats (partial-tile workspace), xs_cols and u_cols (row pitch of
+ *     the token-operand and VeRA-intermediate slots), sync_ints, pre_floats
+ *     (the owned low-rank rows b + v B', all call slots);
+ *   then SCUTE_PLAN_CALL_FIELDS values per call: blk0, d_in, kdim, d_out,
+ *     krv, rv, kblocks, vkb, n_ft, n_vt, vs_chunks, vs_unit0, tile0, lr_rmax,
+ *     lr_items, lr_item0, vs_x, xs_direct;
+ *   then grid + 1 values: the stream-K range bounds start[0..grid].
+ * *n_out = the number of values the plan has (only the first cap written).
+ * SCUTE_ERR_ARG when no decode step has been launched on the context. */
+#define SCUTE_PLAN_HEAD 19
+#define SCUTE_PLAN_CALL_FIELDS 18
+scute_status scute_debug_step_plan(const scute_ctx *ctx, int64_t *out, int cap, int *n_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -120,6 +120,8 @@ _SIGS = {
     "scute_debug_inject": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "scute_debug_fail_alloc": (None, [ctypes.c_int]),
     "scute_set_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "scute_debug_step_plan": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int)]),
     "scute_timing_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int)]),
     "scute_timing_kinds": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -363,6 +365,18 @@ def scute_set_variant(ctx, flags: int) -> None:
     """Place OFT's rotation (1) and / or DoRA's and (IA)^3's s (2) in launches
     of their own around the decode step (byte-model validation)."""
     _check(ctx, load().scute_set_variant(ctx, int(flags)))
+
+
+PLAN_HEAD, PLAN_CALL_FIELDS = 19, 18
+
+
+def scute_debug_step_plan(ctx) -> list:
+    """The last decode-step launch's plan as a list of ints (layout in scute.h)."""
+    n = ctypes.c_int()
+    _check(ctx, load().scute_debug_step_plan(ctx, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_int64 * max(n.value, 1))()
+    _check(ctx, load().scute_debug_step_plan(ctx, buf, n.value, ctypes.byref(n)))
+    return [int(buf[i]) for i in range(n.value)]
 
 
 def scute_debug_fail_alloc(k: int) -> None:

@@ -98,6 +98,26 @@ scute_status grow(scute_ctx *c, void **buf, size_t *cols, size_t need_cols, size
     return SCUTE_OK;
 }
 
+// The decode step's owned low-rank rows b + v B': every call slot holds
+// ceil(largest owned rank / 8) planes of STEP_MAX_TOKENS rows of the widest
+// layer's d_out (fp32).  extra_rank: the rank of an adapter being registered.
+static scute_status grow_pre(scute_ctx *c, int extra_rank) {
+    if (c->dtype != SCUTE_BF16) return SCUTE_OK;   // fp32 contexts never run the decode step
+    int max_dout = 0, max_rank = extra_rank;
+    for (const auto &L : c->layers)
+        if (L.present && L.d_out > max_dout) max_dout = L.d_out;
+    for (const auto &a : c->adapters)
+        if (a.used)
+            for (const auto &al : a.layers)
+                if (al.rank > max_rank) max_rank = al.rank;
+    if (max_dout == 0 || max_rank == 0) return SCUTE_OK;
+    const size_t need = (size_t)STEP_MAX_CALLS * (size_t)((max_rank + 7) / 8) * STEP_MAX_TOKENS * (size_t)max_dout;
+    void *p = c->step_pre;
+    const scute_status st = grow(c, &p, &c->step_pre_floats, need, sizeof(float), 1);
+    c->step_pre = reinterpret_cast<float *>(p);
+    return st;
+}
+
 scute_status remap_workspace(scute_ctx *c) {
     for (auto &L : c->layers) {
         if (!L.present) continue;
@@ -216,7 +236,6 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               dev_malloc((void **)&c->v_part, sizeof(float) * KS_MAX * (size_t)max_tokens * MAX_RANK) == cudaSuccess &&
               dev_malloc((void **)&c->st_ids, sizeof(int32_t) * max_tokens) == cudaSuccess &&
               dev_malloc((void **)&c->gpart, sizeof(float) * PART_WORKSPACE_FLOATS) == cudaSuccess &&
-              dev_malloc((void **)&c->step_v, sizeof(float) * STEP_MAX_CALLS * STEP_MAX_TOKENS * MAX_RANK) == cudaSuccess &&
               dev_malloc((void **)&c->step_sync, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
               cudaMemset(c->step_sync, 0, sizeof(int) * STEP_SYNC_INTS) == cudaSuccess &&
               cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) ==
@@ -243,7 +262,7 @@ void scute_destroy(scute_ctx *c) {
         if (a.storage) cudaFree(a.storage);
     void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
-                    c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_v, c->step_part,
+                    c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_pre, c->step_part,
                     c->step_sync, c->step_hx, c->step_hout, c->var_x};
     for (void *p : bufs)
         if (p) cudaFree(p);
@@ -305,6 +324,7 @@ scute_status scute_add_layer(scute_ctx *c, int layer, int d_in, int d_out, const
         void *pp = c->step_part;
         if (!st) st = grow(c, &pp, &c->step_part_floats, slots * 2 * 128 * c->step_bn_max, 4, 1);
         c->step_part = reinterpret_cast<float *>(pp);
+        if (!st) st = grow_pre(c, 0);
     }
     if (st) {
         // the layer is not added; buffers that did grow have moved, so the
@@ -449,6 +469,13 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
     DeviceGuard dg(c->device);
     scute_status st = ensure_tmp(c, tmp_need ? tmp_need : 256);
     if (st) return st;
+    {
+        int new_rank = 0;
+        for (const auto &al : info)
+            if (al.rank > new_rank) new_rank = al.rank;
+        st = grow_pre(c, new_rank);
+        if (st) return st;
+    }
     void *storage = nullptr;
     CU_TRY(c, dev_malloc(&storage, total ? total : 256));
     uint8_t *cur = reinterpret_cast<uint8_t *>(storage);
@@ -653,7 +680,7 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         k.xs = reinterpret_cast<uint8_t *>(c->step_xs) + (size_t)i * STEP_MAX_TOKENS * c->step_xs_cols * c->esz;
         k.U = vera_on ? reinterpret_cast<uint8_t *>(c->step_U) + (size_t)i * STEP_MAX_TOKENS * c->step_u_cols * c->esz
                       : nullptr;
-        k.v = c->step_v + (size_t)i * STEP_MAX_TOKENS * MAX_RANK;
+        k.pre = c->step_pre ? c->step_pre + (size_t)i * (c->step_pre_floats / STEP_MAX_CALLS) : nullptr;
         k.out = calls[i].out;
         k.slots = c->d_slots + (size_t)calls[i].layer * c->max_adapters;
         k.Wt = L.Wt;
@@ -665,14 +692,20 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
             k.mapBsh = L.mapBsh;
             if (!encode_map(c, &k.mapU, k.U, (uint64_t)L.krv, (uint64_t)STEP_MAX_TOKENS))
                 return fail(c, SCUTE_ERR_CUDA, "tensor map for the VeRA intermediate failed");
-            // VeRA tokens are never rotated, so their rows of x' are rows of x:
-            // the shrink may read x directly and start before x' is formed
-            // (rows of other tokens are discarded by the shrink's epilogue)
-            k.vs_x = (reinterpret_cast<uintptr_t>(k.x) % 16 == 0 && ((size_t)L.d_in * c->esz) % 16 == 0 &&
-                      encode_map(c, &k.mapX, k.x, (uint64_t)L.d_in, (uint64_t)nn))
-                         ? 1
-                         : 0;
         }
+        // Rows that nothing rotates are rows of x: a layer with no rotation
+        // adapter (or whose rotation ran in its own pass) needs no token
+        // operand copy at all, and its base tiles read x itself from the first
+        // block on.  VeRA tokens are never rotated, so the VeRA shrink reads x
+        // directly in every case and starts before x' is formed (rows of other
+        // tokens are discarded by the shrink's epilogue).
+        // (an injected stall keeps the wait on x', which is what it withholds)
+        const bool direct = (L.n_rot == 0 || oft_pass) && c->inject != SCUTE_INJECT_STALL;
+        const bool x_map = (vera_on || direct) && reinterpret_cast<uintptr_t>(k.x) % 16 == 0 &&
+                           ((size_t)L.d_in * c->esz) % 16 == 0 &&
+                           encode_map(c, &k.mapX, k.x, (uint64_t)L.d_in, (uint64_t)nn);
+        k.vs_x = vera_on && x_map ? 1 : 0;
+        k.xs_direct = direct && x_map ? 1 : 0;
         k.d_in = L.d_in;
         k.kdim = L.kdim;
         k.d_out = L.d_out;
@@ -684,6 +717,9 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         k.n_vt = vera_on ? (L.rv + 127) / 128 : 0;
         k.lr_rmax = L.n_lr > 0 ? max_owned_rank(c, calls[i].layer) : 0;
         if (k.lr_rmax > rmax) rmax = k.lr_rmax;
+        if (k.lr_rmax > 0 && (size_t)((k.lr_rmax + 7) / 8) * STEP_MAX_TOKENS * (size_t)L.d_out >
+                                 c->step_pre_floats / STEP_MAX_CALLS)
+            return fail(c, SCUTE_ERR_UNSUPPORTED, "low-rank row workspace smaller than a call needs");
         k.out_f32 = out_f32;
         k.blk0 = blk;
         blk += (long long)k.n_ft * (k.kblocks + k.vkb);
@@ -698,7 +734,10 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         item += k.lr_items;
     }
     // VeRA shrink units: the shortest K chunk (a power of two >= 16 blocks)
-    // that gives at most one unit per CTA
+    // that gives at most one unit per CTA (a unit per VeRA tile at the least)
+    int vt_total = 0;
+    for (int i = 0; i < nc; ++i) vt_total += a.call[i].n_vt;
+    if (vt_total > G) return fail(c, SCUTE_ERR_UNSUPPORTED, "more VeRA shrink tiles (%d) than CTAs (%d)", vt_total, G);
     int ch = 16, units = 0;
     for (;;) {
         units = 0;
@@ -760,6 +799,26 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         return fail(c, SCUTE_ERR_UNSUPPORTED, "partial-tile workspace too small for this batch");
     if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
     a.variant = c->variant;
+    {
+        // the plan as launched, for scute_debug_step_plan
+        std::vector<int64_t> &P = c->last_plan;
+        P.clear();
+        const int64_t head[SCUTE_PLAN_HEAD] = {nc, nn, BN, S, G, units, ch, tile, item, rmax, blk, a.hold,
+                                               (int64_t)step_smem_bytes(BN, S, rmax), c->smem_optin,
+                                               (int64_t)c->step_part_floats, (int64_t)c->step_xs_cols,
+                                               (int64_t)c->step_u_cols, STEP_SYNC_INTS,
+                                               (int64_t)c->step_pre_floats};
+        P.insert(P.end(), head, head + SCUTE_PLAN_HEAD);
+        for (int i = 0; i < nc; ++i) {
+            const StepCall &k = a.call[i];
+            const int64_t f[SCUTE_PLAN_CALL_FIELDS] = {k.blk0, k.d_in, k.kdim, k.d_out, k.krv, k.rv,
+                                                       k.kblocks, k.vkb, k.n_ft, k.n_vt, k.vs_chunks,
+                                                       k.vs_unit0, k.tile0, k.lr_rmax, k.lr_items,
+                                                       k.lr_item0, k.vs_x, k.xs_direct};
+            P.insert(P.end(), f, f + SCUTE_PLAN_CALL_FIELDS);
+        }
+        P.insert(P.end(), a.start, a.start + G + 1);
+    }
     PassArgs pa;
     memset(&pa, 0, sizeof(pa));
     pa.n_calls = nc;
@@ -1133,6 +1192,15 @@ scute_status scute_timing_read(scute_ctx *c, float *ms, int max, int *n_out) {
     CU_TRY(c, cudaDeviceSynchronize());
     int m = c->t_used < max ? c->t_used : max;
     for (int i = 0; i < m; ++i) CU_TRY(c, cudaEventElapsedTime(&ms[i], c->ev[i][0], c->ev[i][1]));
+    *n_out = m;
+    return SCUTE_OK;
+}
+
+scute_status scute_debug_step_plan(const scute_ctx *c, int64_t *out, int cap, int *n_out) {
+    if (!c || !n_out || cap < 0 || (cap > 0 && !out)) return SCUTE_ERR_ARG;
+    if (c->last_plan.empty()) return SCUTE_ERR_ARG;
+    const int m = (int)c->last_plan.size();
+    for (int i = 0; i < m && i < cap; ++i) out[i] = c->last_plan[i];
     *n_out = m;
     return SCUTE_OK;
 }

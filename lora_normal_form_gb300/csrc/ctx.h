@@ -80,7 +80,8 @@ struct scute_ctx {
     size_t step_xs_cols = 0;
     void *step_U = nullptr;      // VeRA intermediates
     size_t step_u_cols = 0;
-    float *step_v = nullptr;     // owned low-rank intermediates [slot][128][MAX_RANK]
+    float *step_pre = nullptr;   // owned low-rank rows b + v B': per call slot [planes][128][d_out]
+    size_t step_pre_floats = 0;  // capacity (all STEP_MAX_CALLS slots)
     float *step_part = nullptr;  // partial tiles
     size_t step_part_floats = 0;
     int *step_sync = nullptr;    // counters (STEP_SYNC_INTS, zero between launches)
@@ -92,6 +93,7 @@ struct scute_ctx {
     int smem_optin = 0;
     int inject = 0;              // scute_debug_inject, consumed by the next decode launch
     int variant = 0;             // scute_set_variant: slots placed in separate passes
+    std::vector<int64_t> last_plan;   // scute_debug_step_plan: the last decode launch's plan
     void *var_x = nullptr;       // rotated copies of the calls' x (separate rotation pass)
     size_t var_x_cols = 0;
     PFN_encodeTiled encode = nullptr;

@@ -187,12 +187,12 @@ struct StepCall {
     CUtensorMap mapAsh;        // A_sh^T [rv][kdim]
     CUtensorMap mapBsh;        // B_sh^T [d_out][krv]
     CUtensorMap mapU;          // VeRA intermediate [128][krv]
-    CUtensorMap mapX;          // caller input [n][d_in] (VeRA shrink operand when vs_x)
+    CUtensorMap mapX;          // token-operand source [n][d_in] (read directly when vs_x / xs_direct)
     const void *x;             // [n][d_in] token-operand source (the caller's x, or its rotated copy)
     const void *x0;            // [n][d_in] the caller's x (low-rank shrink input)
     void *xs;                  // [128][kdim]
     void *U;                   // [128][krv]
-    float *v;                  // [128][MAX_RANK]
+    float *pre;                // [ceil(lr_rmax / 8)][128][d_out] fp32: b + v B' per group of 8 ranks
     void *out;                 // [n][d_out]
     const Slot *slots;         // the layer's slot row
     const void *Wt;            // W^T base (L2 prefetch)
@@ -210,6 +210,7 @@ struct StepCall {
     int lr_items;              // owned low-rank shrink items
     int lr_item0;              // first low-rank item
     int vs_x;                  // VeRA shrink reads x itself (no wait for x')
+    int xs_direct;             // no row of this call is rotated: the base tiles read x itself
 };
 
 struct StepArgs {

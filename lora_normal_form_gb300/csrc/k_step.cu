@@ -13,8 +13,11 @@
 //   * prologue, on the epilogue warps of every CTA while the weights start to
 //     stream: the ids are ordered by (method, adapter) in shared memory; the
 //     token operand x' (x R_a for rotated rows, x otherwise, kept in token
-//     order) is written per layer; the owned low-rank shrink v = x A'_a runs
-//     per adapter segment;
+//     order) is written per layer (a layer with no rotation adapter needs
+//     none: its base tiles read x itself); the owned low-rank term runs per
+//     adapter segment and group of 8 ranks: the shrink v = x A'_a, then at
+//     once, by the same CTA, the expand b + v B'_a over every output feature
+//     of the layer, into fp32 rows that the tiles' finishers read;
 //   * VeRA shared shrink U = (x' A_sh) * d_a on tcgen05, cut into short
 //     K-chunks that are the first work of many CTAs; a VeRA token is never
 //     rotated, so the chunks read x itself and start at once, and U is written
@@ -26,8 +29,8 @@
 //     of all tiles of all layers are split over the CTAs in contiguous ranges
 //     (stream-K).  The CTA holding a tile's first block finishes it: the CTAs
 //     sharing the tile publish their partial tiles, and the finisher adds them
-//     in CTA order to its own accumulator and applies s, b + v B' (formed one
-//     segment ahead) and the VeRA e in its epilogue.
+//     in CTA order to its own accumulator and applies s, b + v B' and the VeRA
+//     e in its epilogue.
 //
 // Waits between CTAs (token operand written, U written, v written) are
 // counters in global memory, read with acquire loads and bounded in time; the
@@ -78,18 +81,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 struct Ctrl {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t tfull[4];
+    uint64_t tempty[4];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;          // this CTA gave up a wait
     int flag;           // broadcast among the epilogue warps
     int meta_call;      // call whose token metadata is staged (-1: none)
-    int v_call;         // call whose low-rank rows are staged
     int n_seg;
     int bad;
     int warp_tot[EPI_WARPS];
     int n_oft[NCALL], n_lrs[NCALL];
+    int it_call[NCALL];   // calls in the order their low-rank items are dealt
+    int it0[NCALL + 1];   // first item of each call in that order
     int done[NCALL];      // low-rank items this CTA finished per call
 };
 constexpr int CTRL_BYTES = 512;
@@ -350,66 +354,6 @@ __device__ __forceinline__ void add_part(const float *src, float (&acc)[8]) {
     acc[4] += p1.x; acc[5] += p1.y; acc[6] += p1.z; acc[7] += p1.w;
 }
 
-// b + v B' of a tile this CTA finishes, in a call with owned low-rank terms,
-// formed while the K loop streams, in this CTA's own slot of the tile (each
-// thread later reads back only what it wrote).  Takes the segment that starts
-// at stream block b0 (ranges end at mend); returns where it ends, or -1 when a
-// wait gave up.  All epilogue threads call it.
-__device__ __noinline__ long long form_pre(const StepArgs &a, Fixed &fx, Ctrl *ctrl, float *vsm, long long b0,
-                                           long long mend, int me, int et, volatile int *abort_flag,
-                                           const int *gabort) {
-    const MLoc L = mlocate(a, b0);
-    const StepCall &k = a.call[L.c];
-    const long long se = min(mend, L.tb0 + L.nkb);
-    if (b0 != L.tb0 || k.lr_rmax == 0) return se;
-    const int n = a.n;
-    if (ctrl->v_call != L.c) {
-        epi_bar();
-        if (et == 0) ctrl->flag = wait_count(a.sync + SY_LR + L.c, k.lr_items, abort_flag, gabort) ? 1 : 0;
-        epi_bar();
-        if (!ctrl->flag) return -1;
-        for (int e = et; e < n * k.lr_rmax; e += EPI_THREADS) {
-            const int t = e / k.lr_rmax, q = e - t * k.lr_rmax;
-            vsm[t * a.rmax + q] = __ldcg(k.v + (size_t)t * MAX_RANK + q);
-        }
-        if (et == 0) ctrl->v_call = L.c;   // read again only after the barrier below
-        epi_bar();
-    }
-    stage_meta(a, L.c, fx, ctrl, et);
-    const int f0 = L.tile * TILE_M;
-    float *own = a.part + (size_t)(a.n_units + k.tile0 + L.tile + me) * ((size_t)2 * TILE_M * a.bn);
-#pragma unroll 1
-    for (int it = et; it < n * 16; it += EPI_THREADS) {
-        const int t = it >> 4, j0 = f0 + (it & 15) * 8;
-        if (j0 >= k.d_out) continue;
-        const TokMeta &m = fx.tmeta[t];
-        float y[8];
-        ld_vec8(m.b + j0, m.b != nullptr, 0.f, y);
-        const float *vrow = vsm + t * a.rmax;
-#pragma unroll 1
-        for (int q0 = 0; q0 < m.rank; q0 += 16) {
-            uint4 bq[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                if (q0 + q < m.rank) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + j0 + (size_t)(q0 + q) * k.d_out));
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                if (q0 + q < m.rank) {
-                    float bf[8];
-                    unpack8(bq[q], bf);
-                    const float vq = vrow[q0 + q];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
-                }
-            }
-        }
-        float4 *dp = reinterpret_cast<float4 *>(own + (size_t)t * TILE_M + (it & 15) * 8);
-        dp[0] = make_float4(y[0], y[1], y[2], y[3]);
-        dp[1] = make_float4(y[4], y[5], y[6], y[7]);
-    }
-    return se;
-}
-
 // x_i A_rows^T for up to LR_Q rows of A (each [d_in], bf16) and the sorted
 // rows [r0, r1) (tokens perm[r]); emit(token, q, value) once per (row, q).
 // Each of the 256 threads covers 8 consecutive k per pass; a warp reduces its
@@ -494,11 +438,14 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
     uint8_t *sbase = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const int BN = a.bn, S = a.stages, G = a.grid, me = (int)blockIdx.x;
     const int STAGE = P_BYTES + BN * 128;
-    const uint32_t NCOLS = 4u * (uint32_t)BN;
+    // accumulator buffers (a base and a VeRA accumulator each): four when
+    // they fit TMEM's 512 columns, so that the MMA can run up to four
+    // segments ahead of the epilogue warps
+    const int NB = BN <= 64 ? 4 : 2;
+    const uint32_t NCOLS = (uint32_t)(2 * NB * BN);
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(sbase + S * STAGE);
     Fixed &fx = *reinterpret_cast<Fixed *>(sbase + S * STAGE + CTRL_BYTES);
     float *xb = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&fx) + sizeof(Fixed));
-    float *vsm = xb + XB_FLOATS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &ctrl->abort;
     int *sync = a.sync;
@@ -511,13 +458,13 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             ptx::mbar_init(ptx::smem_u32(&ctrl->full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&ctrl->empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NB; ++b) {
             ptx::mbar_init(ptx::smem_u32(&ctrl->tfull[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&ctrl->tempty[b]), EPI_WARPS);
         }
         ptx::mbar_init(ptx::smem_u32(&ctrl->drain), 1);
         ctrl->abort = 0;
-        ctrl->meta_call = ctrl->v_call = -1;
+        ctrl->meta_call = -1;
         ctrl->bad = 0;
         for (int c = 0; c < NCALL; ++c) ctrl->done[c] = 0;
         ptx::fence_mbar_init();
@@ -539,7 +486,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             for (int c = 0; c < a.n_calls; ++c) {
                 ptx::prefetch_tmap(&a.call[c].mapW);
                 ptx::prefetch_tmap(&a.call[c].mapXs);
-                if (a.call[c].vs_x) ptx::prefetch_tmap(&a.call[c].mapX);
+                if (a.call[c].vs_x || a.call[c].xs_direct) ptx::prefetch_tmap(&a.call[c].mapX);
             }
             int stage = 0;
             uint32_t phase = 0;
@@ -548,6 +495,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             // first, ahead of the token operands, slots and partial tiles
             const uint64_t once = ptx::make_policy_evict_first();
             unsigned xs_ok = 0, u_ok = 0;
+            for (int c = 0; c < a.n_calls; ++c)
+                if (a.call[c].xs_direct) xs_ok |= 1u << c;   // read from x: nothing to wait for
             bool ok = true;
             // stages whose weight boxes are issued but whose token-operand
             // boxes wait until the prologue has written that call's x'
@@ -638,7 +587,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     if (b < bm && pend_n == 0 && xs_ready(L.c, false)) {
                         // steady state: the call's x' is written and nothing
                         // waits, so the segment's main blocks take a short path
-                        const CUtensorMap *mW = &k.mapW, *mQ = &k.mapXs;
+                        const CUtensorMap *mW = &k.mapW, *mQ = k.xs_direct ? &k.mapX : &k.mapXs;
                         const int prow = L.tile * TILE_M;
                         for (; b < bm; ++b, ++kb) {
                             const uint32_t eb = ptx::smem_u32(&ctrl->empty[stage]);
@@ -670,7 +619,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                         u_ok |= 1u << L.c;
                     }
                     ok = vb ? issue(&k.mapBsh, L.tile * TILE_M, &k.mapU, (kb - k.kblocks) * 64, L.c, false)
-                            : issue(&k.mapW, L.tile * TILE_M, &k.mapXs, kb * 64, L.c, true);
+                            : issue(&k.mapW, L.tile * TILE_M, k.xs_direct ? &k.mapX : &k.mapXs, kb * 64, L.c,
+                                    !k.xs_direct);
                     ++b;
                     ++kb;
                 }
@@ -715,7 +665,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
                 ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[buf]));
-                if (++buf == 2) { buf = 0; bph ^= 1; }
+                if (++buf == NB) { buf = 0; bph ^= 1; }
                 return true;
             };
             for (int u = me; ok && u < a.n_units; u += G) {
@@ -853,6 +803,28 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                 }
             }
             epi_bar();
+            if (et == 0) {
+                // the batch's low-rank items: (segment, group of 8 ranks) of
+                // every call with owned terms, the calls with the most work
+                // per item (d_in + d_out) first, ties in call order
+                unsigned used = 0;
+                for (int o = 0; o < a.n_calls; ++o) {
+                    int best = 0, bw = -1;
+                    for (int c = 0; c < a.n_calls; ++c) {
+                        const int w = a.call[c].d_in + a.call[c].d_out;
+                        if (!((used >> c) & 1u) && w > bw) { bw = w; best = c; }
+                    }
+                    used |= 1u << best;
+                    ctrl->it_call[o] = best;
+                }
+                ctrl->it0[0] = 0;
+                for (int o = 0; o < a.n_calls; ++o) {
+                    const StepCall &k = a.call[ctrl->it_call[o]];
+                    const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
+                    ctrl->it0[o + 1] = ctrl->it0[o] + ctrl->n_lrs[ctrl->it_call[o]] * ng;
+                }
+            }
+            epi_bar();
         }
 
         int buf = 0;
@@ -939,7 +911,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
-            if (++buf == 2) { buf = 0; bph ^= 1; }
+            if (++buf == NB) { buf = 0; bph ^= 1; }
             return true;
         };
 
@@ -954,6 +926,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             int ubase = 0;
             for (int c = 0; c < a.n_calls; ++c) {
                 const StepCall &k = a.call[c];
+                if (k.xs_direct) continue;   // its base tiles read x itself
                 const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x);
                 __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(k.xs);
                 const int ccols = (k.d_in + 255) / 256, units = ccols * ((n + 7) / 8);
@@ -1055,38 +1028,71 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         // the low-rank items, so that the tiles' VeRA blocks wait little
         for (int u = me; ok && u < a.n_units; u += G) ok = unit_epi(u);
 
-        // ---- owned low-rank shrink items (CTA-sized)
-        float *red = xb;   // shrink reduction scratch
-        for (int it = me; it < a.n_items; it += G) {
-            int c = 0, kk = -1;
-            for (int cc = 0; cc < a.n_calls; ++cc) {
-                const StepCall &k = a.call[cc];
-                if (it >= k.lr_item0 && it < k.lr_item0 + k.lr_items) {
-                    c = cc;
-                    kk = it - k.lr_item0;
-                    break;
-                }
-            }
-            if (kk < 0) continue;   // uniform across the CTA
+        // ---- owned low-rank items (CTA-sized): ranks [q0, q0 + 8) of one
+        // adapter segment.  The shrink v = x A' of the segment's rows goes to
+        // shared memory; the expand then runs at once over every output
+        // feature of the layer: plane g = q0 / 8 of the call's rows gets
+        // (b, for g = 0) + sum over those ranks of v_q B'_q, so that the
+        // finishers read b + v B' as the sum of the token's planes, in order.
+        float *red = xb;                        // shrink reduction scratch
+        float *vloc = xb + EPI_WARPS * 32;      // [token][8] v of the current item
+        // Items are dealt round-robin from the last CTA down: the first CTAs
+        // hold the VeRA shrink units, whose epilogues come first.
+        const int n_it = ctrl->it0[a.n_calls];
+        for (int it = G - 1 - me; it < n_it; it += G) {
+            int o = 0;
+            while (it >= ctrl->it0[o + 1]) ++o;
+            const int c = ctrl->it_call[o];
+            const int kk = it - ctrl->it0[o];
             const StepCall &k = a.call[c];
             // the low-rank term acts on x, not on x R (x0: the caller's x even
             // when the token operand comes from a separately rotated copy)
             const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(k.x0);
+            const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
+            const int s_ord = kk / ng, qg = kk - s_ord * ng;   // s_ord < n_lrs[c] by construction
             {
-                // owned low-rank shrink: LR_Q ranks of one segment
-                const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
-                const int s_ord = kk / ng, qg = kk - s_ord * ng;
-                if (s_ord < ctrl->n_lrs[c]) {
-                    const int seg = fx.lr_list[c][s_ord];
-                    const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
-                    const int rk = fx.segRank[c][seg];
-                    const int q0 = qg * LR_Q;
-                    if (q0 < rk) {
-                        const int nq = min(LR_Q, rk - q0);
-                        float *v = k.v;
-                        shrink256(x, k.d_in, fx.perm, r0, r1, fx.segA[c][seg] + (size_t)q0 * k.d_in, nq, red, et,
-                                  [&](int t, int q, float s) { v[(size_t)t * MAX_RANK + q0 + q] = s; });
+                const int seg = fx.lr_list[c][s_ord];
+                const int r0 = fx.seg_start[seg], r1 = fx.seg_start[seg + 1];
+                const int rk = fx.segRank[c][seg];
+                const int q0 = qg * LR_Q;
+                if (q0 < rk) {
+                    const int nq = min(LR_Q, rk - q0);
+                    shrink256(x, k.d_in, fx.perm, r0, r1, fx.segA[c][seg] + (size_t)q0 * k.d_in, nq, red, et,
+                              [&](int t, int q, float v) { vloc[t * LR_Q + q] = v; });
+                    // (shrink256 ends at a barrier: every v of the item is in vloc)
+                    stage_meta(a, c, fx, ctrl, et);
+                    const TokMeta &m = fx.tmeta[fx.perm[r0]];   // the segment's adapter
+                    float *plane = k.pre + (size_t)qg * NTOK * k.d_out;
+#pragma unroll 1
+                    for (int f = et * 8; f < k.d_out; f += EPI_THREADS * 8) {
+                        uint4 bq[LR_Q];
+#pragma unroll
+                        for (int q = 0; q < LR_Q; ++q)
+                            if (q < nq) bq[q] = __ldg(reinterpret_cast<const uint4 *>(m.B + f + (size_t)(q0 + q) * k.d_out));
+                        float bb[8];
+                        ld_vec8(m.b + f, qg == 0 && m.b != nullptr, 0.f, bb);
+#pragma unroll 1
+                        for (int r = r0; r < r1; ++r) {
+                            const int t = fx.perm[r];
+                            float y[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) y[e] = bb[e];
+#pragma unroll
+                            for (int q = 0; q < LR_Q; ++q) {
+                                if (q < nq) {
+                                    float bf[8];
+                                    unpack8(bq[q], bf);
+                                    const float vq = vloc[t * LR_Q + q];
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) y[e] = fmaf(vq, bf[e], y[e]);
+                                }
+                            }
+                            float4 *dp = reinterpret_cast<float4 *>(plane + (size_t)t * k.d_out + f);
+                            dp[0] = make_float4(y[0], y[1], y[2], y[3]);
+                            dp[1] = make_float4(y[4], y[5], y[6], y[7]);
+                        }
                     }
+                    epi_bar();   // vloc is rewritten by the next item
                 }
             }
             if (et == 0) ++ctrl->done[c];
@@ -1101,7 +1107,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         epi_bar();
 
         // ---- epilogues, one per segment of this CTA's work, in issue order
-        long long pre_to = ms;   // segments that start before pre_to have their b + v B'
+        unsigned lr_ok = 0;      // calls whose b + v B' rows this CTA has waited for
         for (long long b = ms; ok && b < mend;) {
             const MLoc L = mlocate(a, b);
             const StepCall &k = a.call[L.c];
@@ -1115,13 +1121,15 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             // higher-numbered ones, and nothing waits in a cycle.
             const bool fin = b == L.tb0;
             float *own = a.part + (size_t)(a.n_units + gtile + me) * SLOT;
-            // b + v B' for this segment's tile and the next one's: the next
-            // tile's is ready before its (possibly short) K loop ends
-            while (ok && pre_to < mend && pre_to <= se) {
-                pre_to = form_pre(a, fx, ctrl, vsm, pre_to, mend, me, et, abort_flag, gabort);
-                if (pre_to < 0) ok = false;
+            if (fin && k.lr_rmax > 0 && !((lr_ok >> L.c) & 1u)) {
+                // b + v B' rows of the call: every low-rank item done
+                epi_bar();
+                const int n_lr_items = ctrl->n_lrs[L.c] * ((k.lr_rmax + LR_Q - 1) / LR_Q);
+                if (et == 0) ctrl->flag = wait_count(sync + SY_LR + L.c, n_lr_items, abort_flag, gabort) ? 1 : 0;
+                epi_bar();
+                if (!ctrl->flag) { ok = false; break; }
+                lr_ok |= 1u << L.c;
             }
-            if (!ok) break;
             const int lastc = fin ? owner(fx, G, L.tb0 + L.nkb - 1) : me;
             if (!epi_all(wait_bar(ptx::smem_u32(&ctrl->tfull[buf]), bph, abort_flag, gabort, true, true))) { ok = false; break; }
             ptx::tc_fence_after();
@@ -1165,12 +1173,15 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                             ld_vec8(m.ve + j0, live[p] && m.vera && m.ve != nullptr, 0.f, e8[p]);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) { oth[p][e] = 0.f; voth[p][e] = 0.f; }
-                            if (k.lr_rmax == 0) {
-                                ld_vec8(m.b + j0, live[p] && m.b != nullptr, 0.f, p8[p]);
-                            } else {
+                            if (live[p] && m.rank > 0) {
+                                // b + v B': the token's rank-group planes, in order
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) p8[p][e] = 0.f;
-                                if (live[p]) add_part(own + (size_t)t[p] * TILE_M + g[p] * 8, p8[p]);   // written by this thread
+#pragma unroll 1
+                                for (int pg = 0; pg * LR_Q < m.rank; ++pg)
+                                    add_part(k.pre + ((size_t)pg * NTOK + t[p]) * k.d_out + j0, p8[p]);
+                            } else {
+                                ld_vec8(m.b + j0, live[p] && m.b != nullptr, 0.f, p8[p]);
                             }
                         }
                         // the sharers' partial tiles, in CTA order
@@ -1229,7 +1240,6 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
                         const int tl = c32 * 32 + ((et & 127) >> 2);
                         if (tl < n) {
                             const size_t off = (size_t)tl * TILE_M + (et & 3) * 32 + (et < 128 ? 0 : (size_t)TILE_M * BN);
-                            if (et < 128 && k.lr_rmax > 0) ptx::discard_l2(own + off);
 #pragma unroll 1
                             for (int j = me + 1; j <= lastc; ++j) {
                                 if (fx.start[j + 1] <= fx.start[j]) continue;
@@ -1246,7 +1256,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[buf]));
-            if (++buf == 2) { buf = 0; bph ^= 1; }
+            if (++buf == NB) { buf = 0; bph ^= 1; }
             b = se;
         }
     }
@@ -1288,8 +1298,8 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
 }  // namespace
 
 size_t step_smem_bytes(int bn, int stages, int rmax) {
-    return 1024 + (size_t)stages * (P_BYTES + bn * 128) + CTRL_BYTES + sizeof(Fixed) + XB_FLOATS * sizeof(float) +
-           (size_t)bn * rmax * sizeof(float);
+    (void)rmax;   // the low-rank intermediates live in the transposition scratch
+    return 1024 + (size_t)stages * (P_BYTES + bn * 128) + CTRL_BYTES + sizeof(Fixed) + XB_FLOATS * sizeof(float);
 }
 
 cudaError_t launch_step(const StepArgs &a, cudaStream_t st) {

@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
 the same seeded inputs.  Indexing is compared bit for bit; floating point is
 graded with the tolerances in ``metrics``."""
+import copy
+
 import numpy as np
 import pytest
 
@@ -160,6 +162,69 @@ def test_separate_pass_variants(scute, variant, out_dtype):
     n0 = ctx.launch_count()
     outs = _batch_run(ctx, w, names, out_dtype)
     assert ctx.launch_count() - n0 == 1 + (variant & 1) + (variant >> 1)
+    assert ctx.sync_status() == 0
+    for name, o in zip(names, outs):
+        H.grade(w, name, o, out_dtype)
+    ctx.close()
+
+
+def _plan_check(ctx, w, names, n):
+    """The library's recorded plan of its last decode launch equals the host
+    restatement (tests/step_plan.py), whose range check then covers it."""
+    import step_plan as SP
+    from lora_normal_form_gb300 import scute_debug_step_plan
+    rec = SP.parse(scute_debug_step_plan(ctx.handle))
+    shapes = SP.layer_shapes(w, names)
+    all_shapes = SP.layer_shapes(w, [L.name for L in w.layers if L.name in ctx.layer_ids])
+    ws = SP.workspace(all_shapes, ctx.max_tokens, rec.head["grid"])
+    mine = SP.plan(shapes, n, torch.cuda.get_device_properties(0).multi_processor_count, ws,
+                   smem_optin=rec.head["smem_optin"])
+    assert rec.head == mine.head
+    assert rec.calls == [{key: k[key] for key in SP.CALL_KEYS} for k in mine.calls]
+    assert rec.start == mine.start
+    SP.audit(rec, SP.seg_lr_counts(w, names, w.ids[:n]))
+
+
+def test_step_plan_matches_restatement(decode_full, scute):
+    """The bench launch's plan (six Llama-3-8B projections, 64 tokens) and a
+    small-shape batch with a repeated layer: recorded plan == restated plan,
+    and every plan-derived index of the kernel in range."""
+    w, ctx, _, _ = decode_full
+    _batch_run(ctx, w, FULL, "bf16")
+    assert ctx.sync_status() == 0
+    _plan_check(ctx, w, list(FULL), w.n)
+    ws = _small_decode(50)
+    c2 = H.make_ctx(scute, ws)
+    names = list(SMALL_NAMES) + ["q"]
+    _batch_run(c2, ws, names, "bf16")
+    assert c2.sync_status() == 0
+    _plan_check(c2, ws, names, ws.n)
+    c2.close()
+
+
+def _without_rotation_on(w, layers):
+    """The same workload with every R slot of the given layers removed: those
+    layers then have no rotation adapter (an OFT adapter is the identity there)."""
+    ads = []
+    for a in w.adapters:
+        b = copy.copy(a)
+        b._gen = {k: g for k, g in a._gen.items() if not (k[1] == "R" and k[0] in layers)}
+        b._cache = {}
+        b.layers = tuple(name for name in a.layers if b.slots(name))
+        ads.append(b)
+    return WL.Workload(w.name + "_norot", w.dtype, w.n, w.ids, w.layers, ads, recipe=w.recipe)
+
+
+@pytest.mark.parametrize("norot", [("k", "down"), tuple(SMALL_NAMES)])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_batch_layers_without_rotation(scute, norot, out_dtype):
+    """A layer with no rotation adapter reads x itself as the token operand
+    (no copy, no wait); in one batch with layers that do rotate, every call is
+    still the oracle's."""
+    w = _without_rotation_on(_small_decode(50), set(norot))
+    ctx = H.make_ctx(scute, w)
+    names = list(SMALL_NAMES)
+    outs = _batch_run(ctx, w, names, out_dtype)
     assert ctx.sync_status() == 0
     for name, o in zip(names, outs):
         H.grade(w, name, o, out_dtype)
