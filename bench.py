@@ -899,11 +899,12 @@ def main():
     del g_mixed, g_lora, g_grouped, g_calls, g_timed
     torch.cuda.empty_cache()
     if rank == 0 and world == 1:
-        for key, skip, fn in (("prefill", args.no_prefill, prefill_leg), ("scaling", args.no_scaling, scaling_leg),
+        for key, skip, fn in (("prefill", args.no_prefill, prefill_leg), ("adapter_scaling", args.no_scaling, scaling_leg),
                               ("stack", args.no_stack, stack_leg),
                               ("time_model_validation", args.no_validation, validation_leg)):
             if skip:
                 continue
+            assert key not in line, key   # a leg never replaces a key of the line's contract
             try:
                 line[key] = fn(scute, dev, flush, launch_us)
             except Exception as exc:   # the headline line is printed whatever a leg does
