@@ -800,6 +800,24 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
     if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
     a.variant = c->variant;
     {
+        // low-rank items are dealt with the calls of most work per item
+        // (d_in + d_out) first, ties in call order
+        unsigned used = 0;
+        for (int o = 0; o < nc; ++o) {
+            int best = 0, bw = -1;
+            for (int i = 0; i < nc; ++i) {
+                const int w = a.call[i].d_in + a.call[i].d_out;
+                if (!((used >> i) & 1u) && w > bw) {
+                    bw = w;
+                    best = i;
+                }
+            }
+            used |= 1u << best;
+            a.it_call[o] = best;
+            a.it_ng[o] = (a.call[best].lr_rmax + 7) / 8;
+        }
+    }
+    {
         // the plan as launched, for scute_debug_step_plan
         std::vector<int64_t> &P = c->last_plan;
         P.clear();

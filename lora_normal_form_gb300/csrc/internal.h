@@ -227,9 +227,11 @@ struct StepArgs {
     int vs_ch;                 // K blocks per VeRA shrink unit
     int n_tiles;               // main tiles over all calls
     int n_items;               // prologue items over all calls
-    int rmax;                  // largest lr_rmax (shared-memory v rows)
+    int rmax;                  // largest lr_rmax
     int hold;                  // extra count the token-operand wait needs (failure-path test)
     int variant;               // VARIANT_*: slots applied by separate passes instead
+    int it_call[STEP_MAX_CALLS];   // calls in the order their low-rank items are dealt
+    int it_ng[STEP_MAX_CALLS];     // rank groups of 8 per owned-term segment, in that order
     long long start[STEP_MAX_GRID + 1];   // main-block range of each CTA: [start[i], start[i+1])
 };
 

@@ -92,8 +92,7 @@ struct Ctrl {
     int bad;
     int warp_tot[EPI_WARPS];
     int n_oft[NCALL], n_lrs[NCALL];
-    int it_call[NCALL];   // calls in the order their low-rank items are dealt
-    int it0[NCALL + 1];   // first item of each call in that order
+    int it0[NCALL + 1];   // first low-rank item of each call, in the order a.it_call
     int done[NCALL];      // low-rank items this CTA finished per call
 };
 constexpr int CTRL_BYTES = 512;
@@ -805,23 +804,14 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
             epi_bar();
             if (et == 0) {
                 // the batch's low-rank items: (segment, group of 8 ranks) of
-                // every call with owned terms, the calls with the most work
-                // per item (d_in + d_out) first, ties in call order
-                unsigned used = 0;
-                for (int o = 0; o < a.n_calls; ++o) {
-                    int best = 0, bw = -1;
-                    for (int c = 0; c < a.n_calls; ++c) {
-                        const int w = a.call[c].d_in + a.call[c].d_out;
-                        if (!((used >> c) & 1u) && w > bw) { bw = w; best = c; }
-                    }
-                    used |= 1u << best;
-                    ctrl->it_call[o] = best;
-                }
+                // every call with owned terms, in the host's order of the calls
+                // (most work per item first); a.it_ng: rank groups per segment
+                int acc = 0;
                 ctrl->it0[0] = 0;
-                for (int o = 0; o < a.n_calls; ++o) {
-                    const StepCall &k = a.call[ctrl->it_call[o]];
-                    const int ng = (k.lr_rmax + LR_Q - 1) / LR_Q;
-                    ctrl->it0[o + 1] = ctrl->it0[o] + ctrl->n_lrs[ctrl->it_call[o]] * ng;
+#pragma unroll
+                for (int o = 0; o < NCALL; ++o) {
+                    if (o < a.n_calls) acc += ctrl->n_lrs[a.it_call[o]] * a.it_ng[o];
+                    ctrl->it0[o + 1] = acc;
                 }
             }
             epi_bar();
@@ -1042,7 +1032,7 @@ __global__ void __launch_bounds__(THREADS, 1) step_kernel(const __grid_constant_
         for (int it = G - 1 - me; it < n_it; it += G) {
             int o = 0;
             while (it >= ctrl->it0[o + 1]) ++o;
-            const int c = ctrl->it_call[o];
+            const int c = a.it_call[o];
             const int kk = it - ctrl->it0[o];
             const StepCall &k = a.call[c];
             // the low-rank term acts on x, not on x R (x0: the caller's x even
