@@ -69,10 +69,16 @@ cudaError_t dev_malloc(void **p, size_t bytes) {
     return cudaMalloc(p, bytes);
 }
 
+bool encode_map_box(scute_ctx *c, CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, int box_rows);
+
 bool encode_map(scute_ctx *c, CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
+    return encode_map_box(c, m, base, inner, rows, 64);
+}
+
+bool encode_map_box(scute_ctx *c, CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, int box_rows) {
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {inner * (uint64_t)c->esz};
-    const cuuint32_t box[2] = {(cuuint32_t)(128 / c->esz), 64};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / c->esz), (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = c->encode(m, c->esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                                  2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -228,6 +234,7 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               dev_malloc((void **)&c->d_seg_start, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_unit, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
+              dev_malloc((void **)&c->d_seg_tile, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
               dev_malloc((void **)&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
               cudaMemset(c->d_meta, 0, sizeof(IndexMeta)) == cudaSuccess &&
               dev_malloc((void **)&c->d_status, sizeof(int)) == cudaSuccess &&
@@ -260,7 +267,7 @@ void scute_destroy(scute_ctx *c) {
     }
     for (auto &a : c->adapters)
         if (a.storage) cudaFree(a.storage);
-    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit,
+    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit, c->d_seg_tile,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
                     c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_pre, c->step_part,
                     c->step_sync, c->step_hx, c->step_hout, c->var_x};
@@ -454,6 +461,7 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
         if (al.R) total += align256((size_t)L.d_in * OFT_BLK * E) * (c->dtype == SCUTE_BF16 ? 2 : 1);
         if (al.rank) {
             total += align256((size_t)al.rank * L.d_in * E) + align256((size_t)al.rank * L.d_out * E);
+            if (c->dtype == SCUTE_BF16) total += align256(sizeof(CUtensorMap));   // A' map of the shrink
             // DoRA also keeps B' without its s (read only by the separate-s-pass placement)
             if (method == SCUTE_DORA) total += align256((size_t)al.rank * L.d_out * E);
             size_t need = align256((size_t)L.d_in * al.rank * E) + align256((size_t)al.rank * L.d_out * E) +
@@ -541,6 +549,18 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
             s.A = Ap;
             s.B = Bp;
             s.rank = al.rank;
+            if (c->dtype == SCUTE_BF16) {
+                // the tensor-core shrink reads A' through a map of its own:
+                // 64 columns x the rank rounded up to 16 rows per box
+                CUtensorMap hm;
+                if (!encode_map_box(c, &hm, Ap, (uint64_t)L.d_in, (uint64_t)al.rank, (al.rank + 15) & ~15)) {
+                    cudaFree(storage);
+                    return fail(c, SCUTE_ERR_CUDA, "tensor map for A' failed");
+                }
+                void *mp = take(sizeof(CUtensorMap));
+                REG_TRY(cudaMemcpy(mp, &hm, sizeof(CUtensorMap), cudaMemcpyHostToDevice));
+                s.mapA = mp;
+            }
         }
         if (method == SCUTE_IA3) {
             float *sp = reinterpret_cast<float *>(take(4 * (size_t)L.d_out));
@@ -609,6 +629,7 @@ scute_status scute_register_adapter(scute_ctx *c, scute_method method, const scu
         if (al.rank) ++L.n_lr;
         if (al.vera) ++L.n_vera;
         if (al.R) ++L.n_rot;
+        if (al.R && al.rank) ++L.n_rot_lr;
     }
     *id_out = id;
     return SCUTE_OK;
@@ -631,6 +652,7 @@ scute_status scute_unregister_adapter(scute_ctx *c, int32_t id) {
         if (al.rank) --L.n_lr;
         if (al.vera) --L.n_vera;
         if (al.R) --L.n_rot;
+        if (al.R && al.rank) --L.n_rot_lr;
     }
     CU_TRY(c, cudaFree(a.storage));
     a = AdapterRec();
@@ -909,7 +931,7 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         // 1. token indexing
         CU_TRY(c, tl.begin());
         CU_TRY(c, launch_index(ids, nn, c->d_method, c->max_adapters, c->d_perm, c->d_aid, c->d_seg_start,
-                               c->d_seg_aid, c->d_meta, c->d_status, st, c->d_seg_unit));
+                               c->d_seg_aid, c->d_meta, c->d_status, st, c->d_seg_unit, c->d_seg_tile));
         CU_TRY(c, tl.end(SCUTE_KIND_INDEX));
         ++k;
         // 2. rotation prologue into the sorted token operand
@@ -965,10 +987,34 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     ++k;
     // 4. owned low-rank shrink / expand
     if (L.n_lr > 0) {
+        // bf16: the shrink on the tensor cores over the sorted token operand,
+        // which holds x itself for every owned-term row unless an adapter of
+        // the layer has both a rotation and an owned term
+        const bool tc = !f32 && L.n_rot_lr == 0;
         CU_TRY(c, tl.begin());
+        if (tc) {
+            LrTcArgs q;
+            memset(&q, 0, sizeof(q));
+            q.mapX = L.mapXs;
+            q.kblocks = (L.d_in + 63) / 64;
+            int kchunk = 0;
+            q.ks = lowrank_ks(L.d_in, &kchunk);
+            q.chunk_blocks = kchunk / 64;
+            q.max_tokens = c->max_tokens;
+            q.seg_start = c->d_seg_start;
+            q.seg_aid = c->d_seg_aid;
+            q.seg_tile = c->d_seg_tile;
+            q.meta = c->d_meta;
+            q.slots = slots;
+            q.v_part = c->v_part;
+            q.status = c->d_status;
+            const int tile_bound = (nn + SEG_TILE_ROWS - 1) / SEG_TILE_ROWS + (reg + 1 < nn ? reg + 1 : nn);
+            const int units = tile_bound * q.ks;
+            CU_TRY(c, launch_lr_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
+        }
         CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, unit_bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
                                  c->d_seg_unit, c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
-                                 lr_rmax));
+                                 lr_rmax, !tc));
         CU_TRY(c, tl.end(SCUTE_KIND_LOWRANK));
         k += 2;
     }

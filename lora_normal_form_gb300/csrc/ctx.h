@@ -26,6 +26,7 @@ struct LayerRec {
     int n_lr = 0;         // registered adapters with an owned term here
     int n_vera = 0;       // registered adapters with a VeRA term here
     int n_rot = 0;        // registered adapters with a rotation here
+    int n_rot_lr = 0;     // registered adapters with both a rotation and an owned term here
 };
 
 struct AdapterLayer {
@@ -61,6 +62,7 @@ struct scute_ctx {
     int8_t *d_method = nullptr;
     int *d_perm = nullptr, *d_aid = nullptr, *d_seg_start = nullptr, *d_seg_aid = nullptr;
     int *d_seg_unit = nullptr;   // work units of the segmented low-rank kernels
+    int *d_seg_tile = nullptr;   // 128-row tiles of the tensor-core low-rank shrink
     IndexMeta *d_meta = nullptr;
     int *d_status = nullptr;
     int *d_err = nullptr;

@@ -36,6 +36,7 @@ struct Slot {
     const float *ve;   // VeRA e [d_out]; null = ones
     const void *Rt;    // R with every 32x32 block transposed (bf16 contexts; null = no R)
     const void *Bu;    // DoRA: B' without its s folded in (the separate-s-pass placement)
+    const void *mapA;  // bf16: CUtensorMap of A' (box 64 columns x rank rounded up to 16 rows)
     int rank;          // rank of the owned term (0 = none)
     int pad;
 };
@@ -259,21 +260,44 @@ cudaError_t launch_s_pass(const PassArgs &p, int max_d_out, cudaStream_t st);
 // Token indexing (one CTA).  seg_unit (optional, n_seg + 1 ints): the
 // segmented low-rank kernels' work units, every segment cut into chunks of
 // SEG_UNIT_ROWS sorted rows; seg_unit[s] counts the chunks before segment s.
+// seg_tile (optional, n_seg + 1 ints): the same with SEG_TILE_ROWS rows, the
+// tiles of the tensor-core shrink.
 constexpr int SEG_UNIT_ROWS = 32;
+constexpr int SEG_TILE_ROWS = 128;
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
-                         int *status, cudaStream_t st, int *seg_unit = nullptr);
+                         int *status, cudaStream_t st, int *seg_unit = nullptr, int *seg_tile = nullptr);
 
 cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const int *perm,
                                  const int *aid_s, const Slot *slots, void *xs, int kdim,
                                  cudaStream_t st, bool pdl);
 
 // Segmented owned low-rank shrink and expand over the units of launch_index
-// (unit_bound: a host-side bound on their number).
+// (unit_bound: a host-side bound on their number); with shrink false only the
+// expand runs (its v_part written by the tensor-core shrink below).
 cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int unit_bound, const int *perm,
                            const int *seg_start, const int *seg_aid, const int *seg_unit,
                            const IndexMeta *meta, const Slot *slots, float *v_part, int max_tokens, void *out,
-                           int out_f32, cudaStream_t st, bool pdl, int max_rank);
+                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink = true);
+
+// Segmented owned low-rank shrink on the tensor cores (bf16): units = the
+// SEG_TILE_ROWS-row tiles of launch_index x the K chunks of lowrank_ks, each
+// writing v_part[chunk][sorted row][rank] like the CUDA-core shrink.  Reads the
+// sorted token operand, so it serves layers where no owned-term row is rotated.
+struct LrTcArgs {
+    CUtensorMap mapX;          // sorted token operand [max_tokens][d_in] (box 64 rows x 128 B)
+    int kblocks;               // 64-wide K blocks of d_in
+    int ks;                    // K chunks (lowrank_ks)
+    int chunk_blocks;          // K blocks per chunk
+    int max_tokens;            // row pitch of a v_part chunk
+    const int *seg_start, *seg_aid, *seg_tile;
+    const IndexMeta *meta;
+    const Slot *slots;
+    float *v_part;             // [ks][max_tokens][MAX_RANK]
+    int *status;
+};
+size_t lr_shrink_tc_smem_bytes();
+cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl);
 
 // registration-time kernels
 cudaError_t launch_transpose_w(bool f32, const void *W, int rows, int cols, void *Wt, int kdim,

@@ -110,7 +110,7 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
 __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, const int8_t *method_tab,
                                                      int A, int *perm, int *aid_s, int *seg_start,
                                                      int *seg_aid, IndexMeta *meta, int *status,
-                                                     int *seg_unit) {
+                                                     int *seg_unit, int *seg_tile) {
     extern __shared__ uint32_t sm[];
     uint32_t *bufA = sm;
     uint32_t *bufB = sm + n;
@@ -164,21 +164,24 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     }
     if (tid == 0) seg_start[total] = n;
     __syncthreads();
-    if (seg_unit) {
-        // work units of the segmented kernels: each segment cut into chunks of
-        // SEG_UNIT_ROWS rows; seg_unit[s] = chunks of the segments before s
+    // work units of the segmented kernels: each segment cut into chunks of
+    // `rows` rows; out[s] = chunks of the segments before s
+    auto unit_prefix = [&](int *out, int rows) {
         const int per_s = (total + blockDim.x - 1) / blockDim.x;
         const int s0 = min(total, tid * per_s), s1 = min(total, s0 + per_s);
         int u = 0;
-        for (int q = s0; q < s1; ++q) u += (seg_start[q + 1] - seg_start[q] + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS;
+        for (int q = s0; q < s1; ++q) u += (seg_start[q + 1] - seg_start[q] + rows - 1) / rows;
         int tot_u = 0;
         int ex = block_excl_scan(u, s_warp, &tot_u);
         for (int q = s0; q < s1; ++q) {
-            seg_unit[q] = ex;
-            ex += (seg_start[q + 1] - seg_start[q] + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS;
+            out[q] = ex;
+            ex += (seg_start[q + 1] - seg_start[q] + rows - 1) / rows;
         }
-        if (tid == 0) seg_unit[total] = tot_u;
-    }
+        if (tid == 0) out[total] = tot_u;
+        __syncthreads();   // s_warp is reused by the next prefix
+    };
+    if (seg_unit) unit_prefix(seg_unit, SEG_UNIT_ROWS);
+    if (seg_tile) unit_prefix(seg_tile, SEG_TILE_ROWS);
     if (tid == 0) {
         meta->n_seg = total;
         int off = 0;
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
 
 cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, int max_adapters,
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
-                         int *status, cudaStream_t st, int *seg_unit) {
+                         int *status, cudaStream_t st, int *seg_unit, int *seg_tile) {
     static std::atomic<unsigned long long> attr_done{0};
     {
         const cudaError_t e = allow_max_dynamic_smem(index_kernel, attr_done);
@@ -215,7 +218,7 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, index_kernel, ids, n, method_tab, max_adapters, perm, aid_s,
-                              seg_start, seg_aid, meta, status, seg_unit);
+                              seg_start, seg_aid, meta, status, seg_unit, seg_tile);
 }
 
 }  // namespace scute

@@ -292,7 +292,8 @@ constexpr int RG = 4;   // rows per pass (one slice of B' serves all of them)
 template <typename T, int RM>
 cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int *perm, const int *seg_start,
                       const int *seg_aid, const int *seg_unit, const IndexMeta *meta, const Slot *slots,
-                      float *v_part, int max_tokens, void *out, int out_f32, cudaStream_t st, bool pdl) {
+                      float *v_part, int max_tokens, void *out, int out_f32, cudaStream_t st, bool pdl,
+                      bool shrink) {
     int kchunk = 0;
     const int ks = lowrank_ks(d_in, &kchunk);
     cudaLaunchAttribute attr;
@@ -305,12 +306,15 @@ cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
     static std::atomic<unsigned long long> attr_done{0};
-    cudaError_t e = allow_max_dynamic_smem(lr_shrink_kernel<T>, attr_done);
-    if (e != cudaSuccess) return e;
-    cfg.dynamicSmemBytes = (size_t)LR_GROUP * kchunk * sizeof(T);
-    e = cudaLaunchKernelEx(&cfg, lr_shrink_kernel<T>, x, d_in, perm, seg_start, seg_aid, seg_unit, meta, slots,
-                           v_part, max_tokens, kchunk);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (shrink) {
+        e = allow_max_dynamic_smem(lr_shrink_kernel<T>, attr_done);
+        if (e != cudaSuccess) return e;
+        cfg.dynamicSmemBytes = (size_t)LR_GROUP * kchunk * sizeof(T);
+        e = cudaLaunchKernelEx(&cfg, lr_shrink_kernel<T>, x, d_in, perm, seg_start, seg_aid, seg_unit, meta, slots,
+                               v_part, max_tokens, kchunk);
+        if (e != cudaSuccess) return e;
+    }
     cfg.dynamicSmemBytes = 0;
     cfg.gridDim = dim3((unsigned)unit_bound, (unsigned)((d_out + 2047) / 2048), 1);
     return cudaLaunchKernelEx(&cfg, lr_expand_kernel<T, RM>, (const float *)v_part, ks, max_tokens, d_out, perm,
@@ -322,19 +326,20 @@ cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int
 cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int unit_bound, const int *perm,
                            const int *seg_start, const int *seg_aid, const int *seg_unit,
                            const IndexMeta *meta, const Slot *slots, float *v_part, int max_tokens, void *out,
-                           int out_f32, cudaStream_t st, bool pdl, int max_rank) {
+                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink) {
     if (f32) {
         if (max_rank <= 16)
             return launch_lr<float, 16>((const float *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid, seg_unit,
-                                        meta, slots, v_part, max_tokens, out, out_f32, st, pdl);
+                                        meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
         return launch_lr<float, 64>((const float *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid, seg_unit,
-                                    meta, slots, v_part, max_tokens, out, out_f32, st, pdl);
+                                    meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
     }
     if (max_rank <= 16)
         return launch_lr<__nv_bfloat16, 16>((const __nv_bfloat16 *)x, d_in, d_out, unit_bound, perm, seg_start,
-                                            seg_aid, seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl);
+                                            seg_aid, seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl,
+                                            shrink);
     return launch_lr<__nv_bfloat16, 64>((const __nv_bfloat16 *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid,
-                                        seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl);
+                                        seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
 }
 
 }  // namespace scute

@@ -297,6 +297,26 @@ def test_small_prefill_parity(scute, out_dtype):
     ctx.close()
 
 
+@pytest.mark.parametrize("rank", [1, 8, 24, 64])
+@pytest.mark.parametrize("n", [200, 700])
+def test_tensor_core_shrink_ranks(scute, rank, n):
+    """Layers with no adapter that both rotates and owns a term run the owned
+    shrink on the tensor cores (tiles of up to 128 sorted rows of one segment,
+    A' boxes of the rank rounded up to 16 rows): ranks 1..64, segments shorter
+    and longer than a tile, the ragged small shapes, both output types."""
+    w = WL.prefill_mixed(n_req=max(2, n // 120), lo=20, hi=240, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES,
+                         rank=rank, req_adapters=list(range(max(2, n // 120))))
+    assert w.n > 128
+    assert all("R" not in a.slots(name) or a.method == "oft" for a in w.adapters for name in a.layers)
+    ctx = H.make_ctx(scute, w)
+    for out_dtype in ("bf16", "fp32"):
+        outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
+        assert ctx.sync_status() == 0
+        for name in SMALL_NAMES:
+            H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
 def test_tiny_fp32(scute):
     """fp32 single linear, 16 tokens, one adapter per method: max rel <= 1e-4.
     Also prints the score under the 1e-3 rms(r) floor, the survey's first
