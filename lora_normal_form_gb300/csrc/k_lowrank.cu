@@ -289,6 +289,99 @@ constexpr int RG = 4;   // rows per pass (one slice of B' serves all of them)
     }
 }
 
+// The expand for bf16 outputs and ranks <= 16: the thread's 16 slices of B'
+// stay in registers for every row of the unit, and the next row pair's old
+// outputs are in flight while the current pair is formed.
+__global__ void __launch_bounds__(256, 2) lr_expand16_kernel(const float *__restrict__ v_part, int ks,
+                                                            int max_tokens, int d_out,
+                                                            const int *__restrict__ perm,
+                                                            const int *__restrict__ seg_start,
+                                                            const int *__restrict__ seg_aid,
+                                                            const int *__restrict__ seg_unit,
+                                                            const IndexMeta *__restrict__ meta,
+                                                            const Slot *__restrict__ slots, void *out) {
+    using T = __nv_bfloat16;
+    __shared__ float vs[SEG_UNIT_ROWS][16];
+    ptx::grid_dep_wait();
+    int r0, r1, a;
+    if (!unit_rows(blockIdx.x, seg_start, seg_aid, seg_unit, meta, r0, r1, a)) return;
+    const T *B = reinterpret_cast<const T *>(slots[a].B);
+    const int r = slots[a].rank;
+    if (B == nullptr || r <= 0) return;
+    const int tid = threadIdx.x;
+    const int nr = r1 - r0;
+    for (int e = tid; e < SEG_UNIT_ROWS * 16; e += 256) {
+        const int rr = e / 16, q = e - rr * 16;
+        float v = 0.f;
+        if (rr < nr && q < r) {
+            float pv[KS_MAX];
+#pragma unroll
+            for (int s = 0; s < KS_MAX; ++s)
+                pv[s] = s < ks ? v_part[((size_t)s * max_tokens + r0 + rr) * MAX_RANK + q] : 0.f;
+#pragma unroll
+            for (int s = 0; s < KS_MAX; ++s) v += pv[s];
+        }
+        vs[rr][q] = v;
+    }
+    __syncthreads();
+    const int j0 = (blockIdx.y * 256 + tid) * 8;
+    if (j0 >= d_out) return;
+    // rank <= 16, bf16: the thread's 16 slices of B' stay in registers
+    // for every row of the unit, and the next row pair's old outputs
+    // are in flight while the current pair is formed
+    const __nv_bfloat16 *Bb = reinterpret_cast<const __nv_bfloat16 *>(B) + j0;
+    __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(out);
+    uint4 bq[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        bq[q] = q < r ? *reinterpret_cast<const uint4 *>(Bb + (size_t)q * d_out) : make_uint4(0u, 0u, 0u, 0u);
+    constexpr int RP = 2;   // rows per step
+    uint4 cur[RP], nxt[RP];
+#pragma unroll
+    for (int rr = 0; rr < RP; ++rr)
+        if (rr < nr) cur[rr] = *reinterpret_cast<const uint4 *>(ob + (size_t)perm[r0 + rr] * d_out + j0);
+#pragma unroll 1
+    for (int g = 0; g < nr; g += RP) {
+#pragma unroll
+        for (int rr = 0; rr < RP; ++rr)
+            if (g + RP + rr < nr)
+                nxt[rr] = *reinterpret_cast<const uint4 *>(ob + (size_t)perm[r0 + g + RP + rr] * d_out + j0);
+        // the slices are converted afresh for every row pair: held converted
+        // across the loop they would need 128 registers
+#pragma unroll
+        for (int q = 0; q < 16; ++q) asm volatile("" : "+r"(bq[q].x), "+r"(bq[q].y), "+r"(bq[q].z), "+r"(bq[q].w));
+        float acc[RP][8];
+#pragma unroll
+        for (int rr = 0; rr < RP; ++rr)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[rr][e] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float bv[8];
+            load8(reinterpret_cast<const T *>(&bq[q]), bv);
+#pragma unroll
+            for (int rr = 0; rr < RP; ++rr) {
+                const float vq = vs[(g + rr) & (SEG_UNIT_ROWS - 1)][q];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(vq, bv[e], acc[rr][e]);
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RP; ++rr) {
+            if (g + rr >= nr) continue;
+            __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&cur[rr]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h[e]);
+                h[e] = __floats2bfloat162_rn(f.x + acc[rr][2 * e], f.y + acc[rr][2 * e + 1]);
+            }
+            *reinterpret_cast<uint4 *>(ob + (size_t)perm[r0 + g + rr] * d_out + j0) = cur[rr];
+        }
+#pragma unroll
+        for (int rr = 0; rr < RP; ++rr) cur[rr] = nxt[rr];
+    }
+}
+
 template <typename T, int RM>
 cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int *perm, const int *seg_start,
                       const int *seg_aid, const int *seg_unit, const IndexMeta *meta, const Slot *slots,
@@ -317,6 +410,9 @@ cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int
     }
     cfg.dynamicSmemBytes = 0;
     cfg.gridDim = dim3((unsigned)unit_bound, (unsigned)((d_out + 2047) / 2048), 1);
+    if (sizeof(T) == 2 && RM == 16 && !out_f32)
+        return cudaLaunchKernelEx(&cfg, lr_expand16_kernel, (const float *)v_part, ks, max_tokens, d_out, perm,
+                                  seg_start, seg_aid, seg_unit, meta, slots, out);
     return cudaLaunchKernelEx(&cfg, lr_expand_kernel<T, RM>, (const float *)v_part, ks, max_tokens, d_out, perm,
                               seg_start, seg_aid, seg_unit, meta, slots, out, out_f32);
 }
