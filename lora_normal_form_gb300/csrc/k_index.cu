@@ -147,7 +147,6 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
         const int rank = (int)(key / (uint32_t)A);
         perm[i] = (int)(v & 0xFFFFu);
         aid_s[i] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
-        atomicAdd(&s_count[rank], 1);
         if (i == 0 || (bufA[i - 1] >> 16) != key) ++nflag;
     }
     int total = 0;
@@ -158,11 +157,19 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
             const int rank = (int)(key / (uint32_t)A);
             seg_start[s] = i;
             seg_aid[s] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
-            atomicAdd(&s_segc[rank], 1);
+            bufB[s] = (uint32_t)rank;   // (bufB is free after the second pass)
             ++s;
         }
     }
     if (tid == 0) seg_start[total] = n;
+    __syncthreads();
+    // rows and segments per method, one shared atomic per segment (one per
+    // row would serialise on the few method counters)
+    for (int q = tid; q < total; q += blockDim.x) {
+        const int rank = (int)bufB[q];
+        atomicAdd(&s_count[rank], seg_start[q + 1] - seg_start[q]);
+        atomicAdd(&s_segc[rank], 1);
+    }
     __syncthreads();
     // work units of the segmented kernels: each segment cut into chunks of
     // `rows` rows; out[s] = chunks of the segments before s
