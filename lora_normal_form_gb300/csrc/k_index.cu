@@ -125,10 +125,27 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     if (tid == 0) s_bad = 0;
     if (tid < N_RANKS) { s_count[tid] = 0; s_segc[tid] = 0; }
     const uint32_t base_key = (uint32_t)RANK_BASE * (uint32_t)A;
-    for (int t = tid; t < n; t += blockDim.x) {
-        const int id = ids[t];
-        int m = -1;
-        if (id >= 0 && id < A) m = method_tab[id];
+    // every id of this thread is requested, then every method-table entry:
+    // two rounds of loads instead of two per id
+    // ids per thread, at most: n <= 2048 runs 256 threads, larger n 1024
+    constexpr int PER_T = INDEX_MAX_TOKENS / 1024;
+    static_assert(PER_T * 256 >= 2048, "ids per thread for the 256-thread launch");
+    int idv[PER_T], mv[PER_T];
+#pragma unroll
+    for (int j = 0; j < PER_T; ++j) {
+        const int t = tid + j * (int)blockDim.x;
+        idv[j] = t < n ? ids[t] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < PER_T; ++j) {
+        mv[j] = -1;
+        if (idv[j] >= 0 && idv[j] < A) mv[j] = method_tab[idv[j]];
+    }
+#pragma unroll
+    for (int j = 0; j < PER_T; ++j) {
+        const int t = tid + j * (int)blockDim.x;
+        if (t >= n) break;
+        const int id = idv[j], m = mv[j];
         if (m < 0 && id != -1) s_bad = 1;
         const uint32_t key = m >= 0 ? (uint32_t)m * (uint32_t)A + (uint32_t)id : base_key;
         bufA[t] = (key << 16) | (uint32_t)t;
