@@ -235,6 +235,8 @@ scute_status scute_create(scute_ctx **out, int device, scute_dtype dtype, int ma
               dev_malloc((void **)&c->d_seg_aid, sizeof(int) * max_tokens) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_unit, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
               dev_malloc((void **)&c->d_seg_tile, sizeof(int) * (max_tokens + 1)) == cudaSuccess &&
+              dev_malloc((void **)&c->vs_ctr, sizeof(int) * VS_CTR_INTS) == cudaSuccess &&
+              cudaMemset(c->vs_ctr, 0, sizeof(int) * VS_CTR_INTS) == cudaSuccess &&
               dev_malloc((void **)&c->d_meta, sizeof(IndexMeta)) == cudaSuccess &&
               cudaMemset(c->d_meta, 0, sizeof(IndexMeta)) == cudaSuccess &&
               dev_malloc((void **)&c->d_status, sizeof(int)) == cudaSuccess &&
@@ -267,7 +269,7 @@ void scute_destroy(scute_ctx *c) {
     }
     for (auto &a : c->adapters)
         if (a.storage) cudaFree(a.storage);
-    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit, c->d_seg_tile,
+    void *bufs[] = {c->d_slots, c->d_method, c->d_perm, c->d_aid, c->d_seg_start, c->d_seg_aid, c->d_seg_unit, c->d_seg_tile, c->vs_ctr, c->vs_part,
                     c->d_meta, c->d_status, c->d_err, c->v_part, c->gpart, c->xs, c->U, c->st_x,
                     c->st_out, c->st_ids, c->tmp, c->step_xs, c->step_U, c->step_pre, c->step_part,
                     c->step_sync, c->step_hx, c->step_hout, c->var_x};
@@ -386,6 +388,12 @@ scute_status scute_set_shared(scute_ctx *c, int layer, int rank, const void *A_s
     st = grow(c, &c->U, &c->u_cols, (size_t)krv, c->esz, c->max_tokens);
     if (!st && !f32) st = grow(c, &c->step_U, &c->step_u_cols, (size_t)krv, c->esz,
                                (size_t)STEP_MAX_CALLS * STEP_MAX_TOKENS);
+    if (!st && !f32) {
+        // partial tiles of the tensor-core VeRA shrink (prefill-sized batches)
+        void *vp = c->vs_part;
+        st = grow(c, &vp, &c->vs_part_cols, (size_t)rank, sizeof(float), (size_t)VS_KS * c->max_tokens);
+        c->vs_part = reinterpret_cast<float *>(vp);
+    }
     if (st) {
         cudaFree(Ash);
         cudaFree(Bsh);
@@ -1047,7 +1055,36 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         v.part_stride = (long long)pv.bn * 128;
         v.n_ft = tok_on_p ? (L.rv + pv.bn - 1) / pv.bn : (L.rv + 127) / 128;
         CU_TRY(c, tl.begin());
-        CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
+        if (!f32 && tok_on_p && L.rv % 64 == 0 && c->vs_part_cols >= (size_t)L.rv) {
+            // many VeRA rows: K-split units on the tensor cores, so that every
+            // SM streams (one CTA per 128 x rank tile over all of K leaves most
+            // of them idle)
+            VsTcArgs q;
+            memset(&q, 0, sizeof(q));
+            q.mapX = L.mapXs;
+            q.mapA = L.mapAsh;
+            q.kblocks = (L.d_in + 63) / 64;
+            // at most VS_KS chunks, none of them empty
+            q.chunk_blocks = (q.kblocks + VS_KS - 1) / VS_KS;
+            q.ks = (q.kblocks + q.chunk_blocks - 1) / q.chunk_blocks;
+            q.n_nt = L.rv / 64;
+            q.rv = L.rv;
+            q.ldu = L.krv;
+            q.max_tokens = c->max_tokens;
+            q.meta = c->d_meta;
+            q.aid_s = c->d_aid;
+            q.slots = slots;
+            q.part = c->vs_part;
+            q.ctr = c->vs_ctr;
+            q.U = c->U;
+            q.status = c->d_status;
+            const int units = (nn + 127) / 128 * q.n_nt * q.ks;
+            if (VS_CTR_TILES + (nn + 127) / 128 * q.n_nt > VS_CTR_INTS)
+                return fail(c, SCUTE_ERR_UNSUPPORTED, "VeRA shrink counters too few for this batch");
+            CU_TRY(c, launch_vera_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
+        } else {
+            CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
+        }
         CU_TRY(c, tl.end(SCUTE_KIND_VERA_SHRINK));
 
         GemmArgs e = v;

@@ -63,6 +63,9 @@ struct scute_ctx {
     int *d_perm = nullptr, *d_aid = nullptr, *d_seg_start = nullptr, *d_seg_aid = nullptr;
     int *d_seg_unit = nullptr;   // work units of the segmented low-rank kernels
     int *d_seg_tile = nullptr;   // 128-row tiles of the tensor-core low-rank shrink
+    float *vs_part = nullptr;    // VeRA shrink partial tiles [VS_KS][max_tokens][rv] (prefill, bf16)
+    size_t vs_part_cols = 0;
+    int *vs_ctr = nullptr;       // VeRA shrink tile counters (VS_CTR_INTS, zero between launches)
     IndexMeta *d_meta = nullptr;
     int *d_status = nullptr;
     int *d_err = nullptr;

@@ -297,6 +297,29 @@ struct LrTcArgs {
     int *status;
 };
 size_t lr_shrink_tc_smem_bytes();
+// VeRA shared shrink on the tensor cores for prefill-sized batches (bf16,
+// shared rank a multiple of 64): units of 128 VeRA rows x 64 shared ranks x
+// one of ks K chunks; partial tiles in `part`, the last unit of a tile sums
+// them in chunk order, applies d and writes U (bf16, row = VeRA row).
+// ctr: [VS_CTR_TILES + tiles] ints, zero between launches.
+enum : int { VS_CTR_EXIT = 0, VS_CTR_ABORT = 1, VS_CTR_TILES = 2 };
+constexpr int VS_CTR_INTS = 4096;
+constexpr int VS_KS = 4;               // K chunks
+struct VsTcArgs {
+    CUtensorMap mapX;          // sorted token operand [max_tokens][d_in]
+    CUtensorMap mapA;          // A_sh^T [rv][d_in] (box 64 rows x 128 B)
+    int kblocks, ks, chunk_blocks;
+    int n_nt;                  // rv / 64
+    int rv, ldu, max_tokens;
+    const IndexMeta *meta;     // offset / count of the VeRA rows
+    const int *aid_s;
+    const Slot *slots;
+    float *part;               // [ks][max_tokens][rv]
+    int *ctr;
+    void *U;                   // bf16 [VeRA rows][ldu]
+    int *status;
+};
+cudaError_t launch_vera_shrink_tc(const VsTcArgs &p, int grid, cudaStream_t st, bool pdl);
 cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl);
 
 // registration-time kernels

@@ -274,6 +274,230 @@ __global__ void __launch_bounds__(THREADS, 1) lr_shrink_tc_kernel(const __grid_c
     ptx::grid_dep_launch();
 }
 
+// ---------------------------------------------------------------- VeRA shared shrink
+// U_t = (x_t A_sh) * d_a(t) over the batch's VeRA rows (a contiguous range of
+// the sorted rows), for prefill-sized batches: units of 128 rows x 64 shared
+// ranks x one of ks K chunks, so that even a few hundred VeRA rows keep every
+// SM streaming (one CTA per 128 x rank tile over the whole of K would leave
+// most idle).  Each unit writes its partial tile (fp32) to a workspace and
+// counts itself; the last unit of a tile adds the ks partials in chunk order,
+// applies d and writes U (bf16): the result does not depend on which CTA
+// finishes last.
+__device__ __forceinline__ void vs_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// The same barrier as a vote: true when v holds in all 128 epilogue threads
+// (a wait that some warps see end and others see give up must not split them).
+__device__ __forceinline__ bool vs_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) vera_shrink_tc_kernel(const __grid_constant__ VsTcArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE);
+    __shared__ int s_last;
+    volatile int *abort_flag = &ctrl->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    ptx::grid_dep_wait();   // segments and token rows come from earlier launches
+    const int base = p.meta->offset[RANK_VERA], count = p.meta->count[RANK_VERA];
+    const int n_rt = (count + TILE_ROWS - 1) / TILE_ROWS;
+    const int per_rt = p.n_nt * p.ks;
+    const int n_units = n_rt * per_rt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&ctrl->full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctrl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&ctrl->tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&ctrl->tempty[b]), 4);
+        }
+        ptx::mbar_init(ptx::smem_u32(&ctrl->drain), 1);
+        ctrl->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&p.mapX);
+        ptx::prefetch_tmap(&p.mapA);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&ctrl->tmem_base), 2 * ACC_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+
+    if (warp == 0) {
+        // ================================================= TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            long long issued = 0;
+            for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+                const int rt = u / per_rt, rem = u - rt * per_rt, nt = rem / p.ks, ch = rem - nt * p.ks;
+                const int kb0 = ch * p.chunk_blocks, kb1 = min(p.kblocks, kb0 + p.chunk_blocks);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bar(ptx::smem_u32(&ctrl->empty[stage]), phase ^ 1, abort_flag)) goto prod_done;
+                    const uint32_t fb = ptx::smem_u32(&ctrl->full[stage]);
+                    const uint32_t sX = ptx::smem_u32(smem + stage * STAGE);
+                    ptx::mbar_arrive_expect_tx(fb, (uint32_t)(XB + BOX_BYTES));
+                    ptx::tma_load_2d(sX, &p.mapX, kb * 64, base + rt * TILE_ROWS, fb);
+                    ptx::tma_load_2d(sX + BOX_BYTES, &p.mapX, kb * 64, base + rt * TILE_ROWS + BOX_ROWS, fb);
+                    ptx::tma_load_2d(sX + XB, &p.mapA, kb * 64, nt * 64, fb);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        prod_done:
+            {
+                const int m_max = issued < STAGES ? (int)issued : STAGES;
+                for (int m = 1; m <= m_max; ++m) {
+                    const int s = (stage - m + STAGES) % STAGES;
+                    const uint32_t ph = (s < stage) ? phase : (phase ^ 1);
+                    wait_bar(ptx::smem_u32(&ctrl->full[s]), ph, abort_flag, false);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================= MMA issuer
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_bf16(TILE_ROWS, 64);
+            for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+                const int rt = u / per_rt, rem = u - rt * per_rt, nt = rem / p.ks, ch = rem - nt * p.ks;
+                (void)rt;
+                (void)nt;
+                const int kb0 = ch * p.chunk_blocks, kb1 = min(p.kblocks, kb0 + p.chunk_blocks);
+                if (!wait_bar(ptx::smem_u32(&ctrl->tempty[acc]), acc_phase ^ 1, abort_flag)) goto mma_done;
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * ACC_COLS);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bar(ptx::smem_u32(&ctrl->full[stage]), phase, abort_flag)) goto mma_done;
+                    ptx::tc_fence_after();
+                    const uint32_t sX = ptx::smem_u32(smem + stage * STAGE);
+                    const uint64_t da = sw128_desc(sX), db = sw128_desc(sX + XB);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(ptx::smem_u32(&ctrl->empty[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+        mma_done:
+            ptx::mma_commit(ptx::smem_u32(&ctrl->drain));
+            wait_bar(ptx::smem_u32(&ctrl->drain), 0, abort_flag, false);
+        }
+        __syncwarp();
+    } else {
+        // ================================================= epilogue warps
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 64;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const int rt = u / per_rt, rem = u - rt * per_rt, nt = rem / p.ks, ch = rem - nt * p.ks;
+            if (!vs_all(wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag))) break;
+            ptx::tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
+            float v0[32], v1[32];
+            ptx::tmem_ld32(tb, v0);
+            ptx::tmem_ld32(tb + 32, v1);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[acc]));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            const int i = rt * TILE_ROWS + row;   // VeRA row
+            if (i < count) {
+                float4 *dst = reinterpret_cast<float4 *>(p.part + ((size_t)ch * p.max_tokens + i) * p.rv + nt * 64);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) dst[c] = make_float4(v0[4 * c], v0[4 * c + 1], v0[4 * c + 2], v0[4 * c + 3]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) dst[8 + c] = make_float4(v1[4 * c], v1[4 * c + 1], v1[4 * c + 2], v1[4 * c + 3]);
+            }
+            // count this unit; the last of the tile's ks units finishes it
+            __threadfence();
+            vs_bar();
+            if (et == 0) {
+                int *ctr = p.ctr + VS_CTR_TILES + rt * p.n_nt + nt;
+                const int old = atomicAdd(ctr, 1);
+                s_last = old == p.ks - 1;
+                if (s_last) atomicExch(ctr, 0);   // every unit of the tile has counted
+            }
+            vs_bar();
+            if (s_last && i < count) {
+                __threadfence();
+                float sum[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) sum[c] = 0.f;
+                for (int k = 0; k < p.ks; ++k) {
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(p.part + ((size_t)k * p.max_tokens + i) * p.rv + nt * 64);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 f = __ldcg(src + c);
+                        sum[4 * c] += f.x;
+                        sum[4 * c + 1] += f.y;
+                        sum[4 * c + 2] += f.z;
+                        sum[4 * c + 3] += f.w;
+                    }
+                }
+                const int a = p.aid_s[base + i];
+                const float *vd = a >= 0 ? p.slots[a].vd : nullptr;
+                __nv_bfloat16 *U = reinterpret_cast<__nv_bfloat16 *>(p.U) + (size_t)i * p.ldu + nt * 64;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 pk;
+                    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 8 * c + 2 * e;
+                        const float d0 = vd ? vd[nt * 64 + j] : 0.f, d1 = vd ? vd[nt * 64 + j + 1] : 0.f;
+                        h[e] = __floats2bfloat162_rn(sum[j] * d0, sum[j + 1] * d1);
+                    }
+                    reinterpret_cast<uint4 *>(U)[c] = pk;
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 2 * ACC_COLS);
+    }
+    if (threadIdx.x == 0) {
+        if (ctrl->abort) {
+            atomicOr(p.status, STATUS_TIMEOUT);
+            atomicExch(p.ctr + VS_CTR_ABORT, 1);
+        }
+        // the last CTA out clears the tile counters a launch that gave up left
+        __threadfence();
+        if (atomicAdd(p.ctr + VS_CTR_EXIT, 1) == (int)gridDim.x - 1) {
+            __threadfence();
+            if (atomicAdd(p.ctr + VS_CTR_ABORT, 0) != 0)
+                for (int t = 0; t < n_rt * p.n_nt; ++t) p.ctr[VS_CTR_TILES + t] = 0;
+            p.ctr[VS_CTR_ABORT] = 0;
+            p.ctr[VS_CTR_EXIT] = 0;
+            __threadfence();
+        }
+    }
+    ptx::grid_dep_launch();
+}
+
 }  // namespace
 
 size_t lr_shrink_tc_smem_bytes() { return 1024 + (size_t)STAGES * STAGE + CTRL_BYTES; }
@@ -295,6 +519,25 @@ cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bo
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, lr_shrink_tc_kernel, p);
+}
+
+cudaError_t launch_vera_shrink_tc(const VsTcArgs &p, int grid, cudaStream_t st, bool pdl) {
+    static std::atomic<unsigned long long> attr_done{0};
+    {
+        const cudaError_t e = allow_max_dynamic_smem(vera_shrink_tc_kernel, attr_done);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = lr_shrink_tc_smem_bytes();
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, vera_shrink_tc_kernel, p);
 }
 
 }  // namespace scute

@@ -131,3 +131,25 @@ def test_stream_k_ranges_cover_every_block_once():
     assert (owner >= 0).all()
     for b in range(0, p.head["t_main"], 97):
         assert SP.owner(p, b) == owner[b]
+
+
+def _lowrank_ks(d_in):
+    # the K chunks of the low-rank shrink (csrc/internal.h lowrank_ks)
+    ks = min(-(-d_in // 2048), 8)
+    kchunk = -(-(-(-d_in // ks)) // 256) * 256
+    return -(-d_in // kchunk), kchunk
+
+
+def test_k_chunks_are_never_empty():
+    """Every K chunk of the tensor-core shrinks holds at least one K block, for
+    every input width the library accepts (a chunk with none would hand its
+    partial an accumulator no MMA wrote): the low-rank shrink's chunks and the
+    VeRA shrink's (at most 4)."""
+    for d_in in range(32, 16384 + 1, 32):
+        kblocks = -(-d_in // 64)
+        ks, kchunk = _lowrank_ks(d_in)
+        cb = kchunk // 64
+        assert ks <= 8 and kchunk % 256 == 0 and (ks - 1) * cb < kblocks, d_in
+        vcb = -(-kblocks // 4)
+        vks = -(-kblocks // vcb)
+        assert vks <= 4 and (vks - 1) * vcb < kblocks <= vks * vcb, d_in
