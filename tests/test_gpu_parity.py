@@ -317,6 +317,23 @@ def test_tensor_core_shrink_ranks(scute, rank, n):
     ctx.close()
 
 
+@pytest.mark.parametrize("rv", [96, 1024])
+def test_prefill_vera_shared_ranks(scute, rv):
+    """Prefill-sized batches with VeRA tenants at shared rank 1024 (the largest:
+    16 column tiles of the tensor-core VeRA shrink) and 96 (not a multiple of
+    64: the GEMM path), both output types, ragged shapes."""
+    w = WL.prefill_mixed(n_req=4, lo=60, hi=200, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES, rv=rv,
+                         req_adapters=[3, 8, 0, 13])   # three VeRA requests and a LoRA one
+    assert w.n > 256 and H.methods_in(w, range(w.n)) >= {"vera", "lora"}
+    ctx = H.make_ctx(scute, w)
+    for out_dtype in ("bf16", "fp32"):
+        outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
+        assert ctx.sync_status() == 0
+        for name in SMALL_NAMES:
+            H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
 def test_tiny_fp32(scute):
     """fp32 single linear, 16 tokens, one adapter per method: max rel <= 1e-4.
     Also prints the score under the 1e-3 rms(r) floor, the survey's first
