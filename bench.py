@@ -96,6 +96,10 @@ def parse():
     p.add_argument("--eager-steps", type=int, default=0,
                    help="only run this many untimed batched steps of the mixed workload and exit "
                         "(a fixed launch sequence for profilers); prints no JSON line")
+    p.add_argument("--eager-variant", type=int, default=0, choices=[0, 1, 2, 3],
+                   help="launch placement of the --eager-steps calls: 0 fused, 1 the rotation as its own "
+                        "pass, 2 DoRA's and (IA)^3's s as their own pass, 3 both; the byte model's bytes "
+                        "per launch of that placement go to stderr")
     p.add_argument("--prefill-eager", type=int, default=0,
                    help="only run this many untimed prefill calls (q projection) and exit (profilers)")
     return p.parse_args()
@@ -428,8 +432,10 @@ def prefill_leg(scute, dev, flush, launch_us, steps=6):
                              frac=f / (t * 1e-3) / 1e12 / attainable, bound="tensor" if attainable >= tf_peak else "hbm")
                 else:
                     e.update(frac=e["gbs"] / hbm, bound="hbm")
-                # the time model for this launch (the low-rank pair is two launches)
-                nl = 2 if k == "lowrank" else 1
+                # the time model for this launch (the owned low-rank timing covers
+                # the shrink and, unless the base GEMM's epilogue runs it, the expand)
+                nl = sum(1 for name, _, _ in rep["kernels"] if name in ("lr_shrink", "lr_expand")) \
+                    if k == "lowrank" else 1
                 e["predicted_us"] = max(b / (hbm * 1e3), f / (tf_peak * 1e6)) + nl * launch_us
                 e["model_error_pct"] = 100.0 * abs(1e3 * t - e["predicted_us"]) / (1e3 * t)
                 kern[k] = e
@@ -708,6 +714,10 @@ def main():
         xs = {p: to_dev(w.layer(p).get("x")) for p in PROJ}
         ids = torch.from_numpy(w.ids.copy()).to(dev)
         outs = {p: torch.empty(w.n, w.layer(p).d_out, dtype=torch.bfloat16, device=dev) for p in PROJ}
+        ctx.set_variant(args.eager_variant)
+        rep = ctx.predict_batch([ctx.layer_ids[p] for p in PROJ], w.ids, "bf16")
+        for name, b, _f in rep["kernels"]:
+            print(f"byte model, placement {args.eager_variant}: {name} {b} bytes", file=sys.stderr)
         for _ in range(args.eager_steps):
             ctx.linear_batch([(xs[p], ctx.layer_ids[p], outs[p]) for p in PROJ], ids, "bf16")
         torch.cuda.synchronize()

@@ -949,55 +949,27 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         CU_TRY(c, tl.end(SCUTE_KIND_ROTATE));
         ++k;
     }
-    // 3. base GEMM with the s / b epilogue
     const bool tok_on_p = nn > 256;
+    // bf16 with tokens on the GEMM's 128-row side: the owned low-rank expand
+    // runs in the base GEMM's epilogue (each out row written once), so the
+    // shrink comes first
+    const bool lr_fused = !f32 && tok_on_p && L.n_lr > 0;
     // owned low-rank term: units of SEG_UNIT_ROWS rows of every segment;
     // there are at most n / SEG_UNIT_ROWS + (segments) of them, and at most
     // one segment per registered adapter plus the base rows
     int reg = 0;
     for (const auto &a : c->adapters) reg += a.used ? 1 : 0;
     const int unit_bound = (nn + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS + (reg + 1 < nn ? reg + 1 : nn);
-    GemmArgs g;
-    memset(&g, 0, sizeof(g));
-    g.mapP = tok_on_p ? L.mapXs : L.mapW;
-    g.mapQ = tok_on_p ? L.mapW : L.mapXs;
-    g.kblocks = (L.kdim * c->esz + 127) / 128;
-    g.n_feat = L.d_out;
-    g.tok_on_p = tok_on_p ? 1 : 0;
-    g.n_tok_host = nn;
-    g.epi = EPI_BASE;
-    g.out_f32 = out_f32;
-    g.ld_out = L.d_out;
-    g.slots = slots;
-    g.perm = c->d_perm;
-    g.aid_s = c->d_aid;
-    g.out = out;
-    g.status = c->d_status;
-    if (!tok_on_p) {
-        g.p_base = L.Wt;
-        g.p_pitch = (long long)L.kdim * c->esz;
-        g.p_rows = L.d_out;
+    int lr_ks = 0;
+    {
+        int kchunk = 0;
+        lr_ks = lowrank_ks(L.d_in, &kchunk);
     }
-    GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms, g.lr_rmax);
-    g.splits = p.splits;
-    g.stages = p.stages;
-    g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
-    if (!tok_on_p && p.splits == 1 &&
-        (size_t)p.stages * (128 * 128 + p.bn * 128) < (size_t)(g.vera_kb ? 2 : 1) * p.bn * 132 * 4)
-        return fail(c, SCUTE_ERR_UNSUPPORTED, "the accumulator tile does not fit the pipeline buffers");
-    if (!tok_on_p && p.splits > 1 && gemm_part_floats(p.grid, p.bn, g.vera_kb > 0) > PART_WORKSPACE_FLOATS)
-        return fail(c, SCUTE_ERR_UNSUPPORTED, "K-split workspace too small for this launch");
-    g.part = c->gpart;
-    g.part_stride = (long long)p.bn * 128 * (g.vera_kb ? 2 : 1);
-    CU_TRY(c, tl.begin());
-    CU_TRY(c, launch_gemm(g, p, st, c->pdl));
-    CU_TRY(c, tl.end(SCUTE_KIND_BASE_GEMM));
-    ++k;
-    // 4. owned low-rank shrink / expand
-    if (L.n_lr > 0) {
-        // bf16: the shrink on the tensor cores over the sorted token operand,
-        // which holds x itself for every owned-term row unless an adapter of
-        // the layer has both a rotation and an owned term
+    // owned low-rank shrink (and, unless fused, its expand).  bf16: the shrink
+    // runs on the tensor cores over the sorted token operand, which holds x
+    // itself for every owned-term row unless an adapter of the layer has both
+    // a rotation and an owned term
+    auto owned_lowrank = [&](bool expand) -> scute_status {
         const bool tc = !f32 && L.n_rot_lr == 0;
         CU_TRY(c, tl.begin());
         if (tc) {
@@ -1020,11 +992,68 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
             const int units = tile_bound * q.ks;
             CU_TRY(c, launch_lr_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
         }
-        CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, unit_bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
-                                 c->d_seg_unit, c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st, c->pdl,
-                                 lr_rmax, !tc));
+        if (!tc || expand)
+            CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, unit_bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
+                                     c->d_seg_unit, c->d_meta, slots, c->v_part, c->max_tokens, out, out_f32, st,
+                                     c->pdl, lr_rmax, !tc, expand));
         CU_TRY(c, tl.end(SCUTE_KIND_LOWRANK));
-        k += 2;
+        k += expand ? 2 : 1;
+        return SCUTE_OK;
+    };
+    // 3. owned low-rank shrink, when its expand is fused into the base GEMM
+    if (lr_fused) {
+        const scute_status e = owned_lowrank(false);
+        if (e != SCUTE_OK) return e;
+    }
+    // 4. base GEMM with the s / b (and fused owned low-rank) epilogue
+    GemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.mapP = tok_on_p ? L.mapXs : L.mapW;
+    g.mapQ = tok_on_p ? L.mapW : L.mapXs;
+    g.kblocks = (L.kdim * c->esz + 127) / 128;
+    g.n_feat = L.d_out;
+    g.tok_on_p = tok_on_p ? 1 : 0;
+    g.n_tok_host = nn;
+    g.epi = EPI_BASE;
+    g.out_f32 = out_f32;
+    g.ld_out = L.d_out;
+    g.slots = slots;
+    g.perm = c->d_perm;
+    g.aid_s = c->d_aid;
+    g.out = out;
+    g.status = c->d_status;
+    if (lr_fused) {
+        g.v = c->v_part;
+        g.v_ld = MAX_RANK;
+        g.v_ks = lr_ks;
+        g.v_kstride = (long long)c->max_tokens * MAX_RANK;
+        g.lr_rmax = lr_rmax;
+    }
+    if (!tok_on_p) {
+        g.p_base = L.Wt;
+        g.p_pitch = (long long)L.kdim * c->esz;
+        g.p_rows = L.d_out;
+    }
+    GemmPlan p = plan_gemm(nn, L.d_out, g.kblocks, tok_on_p, f32, c->num_sms, g.lr_rmax);
+    g.splits = p.splits;
+    g.stages = p.stages;
+    g.n_ft = tok_on_p ? (L.d_out + p.bn - 1) / p.bn : (L.d_out + 127) / 128;
+    if (!tok_on_p && p.splits == 1 &&
+        (size_t)p.stages * (128 * 128 + p.bn * 128) < (size_t)(g.vera_kb ? 2 : 1) * p.bn * 132 * 4)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "the accumulator tile does not fit the pipeline buffers");
+    if (!tok_on_p && p.splits > 1 && gemm_part_floats(p.grid, p.bn, g.vera_kb > 0) > PART_WORKSPACE_FLOATS)
+        return fail(c, SCUTE_ERR_UNSUPPORTED, "K-split workspace too small for this launch");
+    g.part = c->gpart;
+    g.part_stride = (long long)p.bn * 128 * (g.vera_kb ? 2 : 1);
+    CU_TRY(c, tl.begin());
+    CU_TRY(c, launch_gemm(g, p, st, c->pdl));
+    CU_TRY(c, tl.end(SCUTE_KIND_BASE_GEMM));
+    ++k;
+    // owned low-rank shrink and expand after the base GEMM (the expand adds
+    // into out): fp32 contexts and the features-on-P orientation
+    if (L.n_lr > 0 && !lr_fused) {
+        const scute_status e = owned_lowrank(true);
+        if (e != SCUTE_OK) return e;
     }
     // 5. VeRA: shared shrink then shared expand over the VeRA rows only
     if (vera_on) {

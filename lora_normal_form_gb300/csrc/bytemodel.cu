@@ -98,17 +98,28 @@ bool count_layer(const scute_bm_layer *L, const int32_t *ids, int64_t n, LayerCo
 
 // The per-kernel plan (fp32 contexts and batches above the decode step's
 // token limit): indexing, rotation into the sorted token operand, base GEMM,
-// owned low-rank shrink and expand, VeRA shrink and expand GEMMs.
+// owned low-rank shrink and expand, VeRA shrink and expand GEMMs.  In bf16
+// contexts with more than 256 tokens the owned shrink runs before the base
+// GEMM and the owned expand inside its epilogue (the GEMM then also reads the
+// partial v and each B', and writes out once).
 void per_kernel_plan(const scute_bm_layer *L, const LayerCount &c, scute_byte_report *rep) {
     const int64_t n = c.n, E = c.E, Eo = c.Eo;
     const int64_t index_out = 8 * n + 4 * (c.segs + 1) + 4 * c.segs + 88;
+    const int64_t ks = scute::lowrank_ks(L->d_in, nullptr);
+    const bool fused = L->lowrank_launched && L->dtype != SCUTE_FP32 && n > 256;
     add_kernel(rep, "index", 4 * n + index_out, 0);
     add_kernel(rep, "rotate", n * c.din * E + 8 * n + c.R + n * c.kd * E, 2 * c.n_rot * c.din * 32);
-    add_kernel(rep, "base_gemm", c.dout * c.kd * E + n * c.kd * E + c.sb + 8 * n + n * c.dout * Eo,
-               2 * n * c.kd * c.dout);
-    if (L->lowrank_launched) {
-        const int64_t ks = scute::lowrank_ks(L->d_in, nullptr);
-        add_kernel(rep, "lr_shrink", c.n_lr * c.din * E + c.A + ks * c.lr_rank_rows * 4, 2 * c.lr_rank_rows * c.din);
+    const int64_t shrink_b = c.n_lr * c.din * E + c.A + ks * c.lr_rank_rows * 4;
+    if (fused) add_kernel(rep, "lr_shrink", shrink_b, 2 * c.lr_rank_rows * c.din);
+    int64_t gemm_b = c.dout * c.kd * E + n * c.kd * E + c.sb + 8 * n + n * c.dout * Eo;
+    int64_t gemm_f = 2 * n * c.kd * c.dout;
+    if (fused) {
+        gemm_b += ks * c.lr_rank_rows * 4 + c.B;
+        gemm_f += 2 * c.lr_rank_rows * c.dout;
+    }
+    add_kernel(rep, "base_gemm", gemm_b, gemm_f);
+    if (L->lowrank_launched && !fused) {
+        add_kernel(rep, "lr_shrink", shrink_b, 2 * c.lr_rank_rows * c.din);
         add_kernel(rep, "lr_expand", ks * c.lr_rank_rows * 4 + c.B + 2 * c.n_lr * c.dout * Eo,
                    2 * c.lr_rank_rows * c.dout);
     }

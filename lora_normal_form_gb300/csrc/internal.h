@@ -35,7 +35,8 @@ struct Slot {
     const float *vd;   // VeRA d [shared rank] (c folded in); null = no shared term
     const float *ve;   // VeRA e [d_out]; null = ones
     const void *Rt;    // R with every 32x32 block transposed (bf16 contexts; null = no R)
-    const void *Bu;    // DoRA: B' without its s folded in (the separate-s-pass placement)
+    const void *Bu;    // DoRA: B' without its s folded in (the separate-s-pass placement,
+                       // and the prefill expand that runs before s is applied)
     const void *mapA;  // bf16: CUtensorMap of A' (box 64 columns x rank rounded up to 16 rows)
     int rank;          // rank of the owned term (0 = none)
     int pad;
@@ -86,11 +87,19 @@ struct GemmArgs {
     void *out;                 // [n, ld_out]
     void *U;                   // VeRA intermediate
     int *status;
-    // fused epilogue (features-on-P orientation only)
-    int vera_kb;               // VeRA expand K blocks folded into this GEMM (0 = none)
-    const float *v;            // owned low-rank intermediate [tokens][v_ld] (null = none)
+    // fused epilogue
+    int vera_kb;               // VeRA expand K blocks folded into this GEMM (0 = none; features on P)
+    // owned low-rank intermediate (null = none).  Features on P: v[row * v_ld + q].
+    // Tokens on P (bf16): the K-chunk partials of the shrink, summed in chunk
+    // order, v[s * v_kstride + row * v_ld + q] for s < v_ks; the expand runs as
+    // an extra tensor-core K block of each tile (rows of adapters with an s
+    // other than DoRA's, or beyond the block's k-steps, on the CUDA cores in
+    // the epilogue), so out is written once
+    const float *v;
     int v_ld;
-    int lr_rmax;               // largest owned rank on the layer (v columns preloaded)
+    int v_ks;
+    long long v_kstride;
+    int lr_rmax;               // largest owned rank on the layer (features on P: v columns per token)
     // the P operand's rows in global memory (features-on-P orientation): each
     // CTA asks L2 for its whole K range of them at start
     const void *p_base;
@@ -274,11 +283,14 @@ cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const
 
 // Segmented owned low-rank shrink and expand over the units of launch_index
 // (unit_bound: a host-side bound on their number); with shrink false only the
-// expand runs (its v_part written by the tensor-core shrink below).
+// expand runs (its v_part written by the tensor-core shrink below), with
+// expand false only the shrink (the expand then runs in the base GEMM's
+// epilogue).
 cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int unit_bound, const int *perm,
                            const int *seg_start, const int *seg_aid, const int *seg_unit,
                            const IndexMeta *meta, const Slot *slots, float *v_part, int max_tokens, void *out,
-                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink = true);
+                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink = true,
+                           bool expand = true);
 
 // Segmented owned low-rank shrink on the tensor cores (bf16): units = the
 // SEG_TILE_ROWS-row tiles of launch_index x the K chunks of lowrank_ks, each

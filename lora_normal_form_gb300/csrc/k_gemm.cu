@@ -41,7 +41,8 @@ constexpr int TILE_M = 128;
 constexpr int BOX_ROWS = 64;
 constexpr int BOX_BYTES = BOX_ROWS * 128;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
-constexpr int CTRL_BYTES = 256;
+constexpr int CTRL_BYTES = 512;
+constexpr size_t GEMM_SMEM_MAX = 227 * 1024;   // dynamic shared memory of one CTA
 // token stride of the partial tiles in shared memory: 128 features plus 4
 // floats of padding, so the tokens a warp reads start on different banks
 constexpr int RED_LD = TILE_M + 4;
@@ -61,6 +62,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for the 64-byte-swizzle layout: rows of 64 bytes, 8-row atoms of
+// 512 bytes (stride byte offset 512); 16-byte unit u of row r sits at unit
+// u ^ ((r >> 1) & 3).  Base 1024-byte aligned; K advances 32 bytes (+2) per
+// 16 bf16 elements.
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused here)
+    d |= (uint64_t)(512 >> 4) << 32;            // stride byte offset
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)4 << 61;                     // 64-byte swizzle
+    return d;
+}
+__device__ __forceinline__ uint32_t sw64_offset(int r, int unit) {
+    return (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((unit ^ ((r >> 1) & 3)) << 4));
+}
+
 // Instruction descriptor: f32 accumulator, A/B bf16 (1) or tf32 (2), both
 // K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t instr_desc(bool tf32, int M, int N) {
@@ -68,14 +86,28 @@ __host__ __device__ constexpr uint32_t instr_desc(bool tf32, int M, int N) {
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Owned low-rank expand on the tensor cores (tokens on P, bf16): per tile one
+// extra K block of LR_KSTEPS x 16 columns, A = the rows' v (each row in the
+// columns of its adapter's k-steps, zeros elsewhere), B = the tile's features
+// of each adapter's B, both K-major in the 64-byte-swizzle layout.
+constexpr int LR_KSTEPS = 2;
+constexpr int LR_A_BYTES = TILE_M * 64;
+
 struct Ctrl {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t lrfull;                // the tile's low-rank operands are in shared memory (128 arrivals)
     uint32_t tmem_base;
     int abort;
+    // per tile parity: k-steps the MMA issues, each k-step's adapter (-2 none),
+    // its first k-step, rank and B, and the epilogue warps' counts of k-steps
+    int lr_steps[2];
+    int lr_aid[2][LR_KSTEPS], lr_k0[2][LR_KSTEPS], lr_rank[2][LR_KSTEPS];
+    int lr_wsum[2][4];
+    const void *lr_B[2][LR_KSTEPS];
 };
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
 
@@ -103,6 +135,8 @@ struct TokMeta {
     const float *v1;       // s (BASE), d (VERA_D), e (VERA_E)
     const float *v2;       // b (BASE)
     const void *B;         // fused owned B' [rank][n_feat] (BASE)
+    const void *Bm;        // tokens on P: B for the tensor-core expand, added before s
+                           // (B' when the adapter has no s, DoRA's B without s; null = none)
     const float *ve;       // fused VeRA e (BASE)
     int rank;              // fused owned rank
     int vera;              // fused: the row is a VeRA row
@@ -115,6 +149,7 @@ __device__ __forceinline__ TokMeta tok_meta(const GemmArgs &g, int i, int sorted
     m.v1 = nullptr;
     m.v2 = nullptr;
     m.B = nullptr;
+    m.Bm = nullptr;
     m.ve = nullptr;
     m.rank = 0;
     m.vera = 0;
@@ -134,6 +169,7 @@ __device__ __forceinline__ TokMeta tok_meta(const GemmArgs &g, int i, int sorted
     m.v2 = sl.b;
     if (g.v && sl.B && sl.rank > 0) {
         m.B = sl.B;
+        m.Bm = sl.s ? sl.Bu : sl.B;
         m.rank = sl.rank;
     }
     if (g.vera_kb && sl.vd) {
@@ -144,7 +180,11 @@ __device__ __forceinline__ TokMeta tok_meta(const GemmArgs &g, int i, int sorted
 }
 
 // 32 consecutive features [j0, j0+32) of one row (tokens-on-P orientation).
-__device__ __forceinline__ void emit32(const GemmArgs &g, const TokMeta &r, int j0, const float (&acc)[32]) {
+// vsrc: the row's K-chunk partials of the owned low-rank intermediate when its
+// expand is added here on the CUDA cores (bf16 contexts; the tensor-core expand
+// did not take the row), else null.
+__device__ __forceinline__ void emit32(const GemmArgs &g, const TokMeta &r, int j0, const float (&acc)[32],
+                                       const float *vsrc) {
     float v[32];
     if (g.epi == EPI_VERA_D) {
 #pragma unroll
@@ -188,6 +228,41 @@ __device__ __forceinline__ void emit32(const GemmArgs &g, const TokMeta &r, int 
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         v[k] = acc[k] * s4.x + b4.x; v[k + 1] = acc[k + 1] * s4.y + b4.y;
         v[k + 2] = acc[k + 2] * s4.z + b4.z; v[k + 3] = acc[k + 3] * s4.w + b4.w;
+    }
+    if (vsrc) {
+        // owned low-rank expand: y += v_t B'[:, j0:j0+32], four ranks per
+        // batch (v summed over the K chunks in chunk order)
+        const __nv_bfloat16 *B = reinterpret_cast<const __nv_bfloat16 *>(r.B) + j0;
+#pragma unroll 1
+        for (int q0 = 0; q0 < r.rank; q0 += 4) {
+            float4 vs = __ldg(reinterpret_cast<const float4 *>(vsrc + q0));
+            for (int s = 1; s < g.v_ks; ++s) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(vsrc + s * g.v_kstride + q0));
+                vs.x += t.x; vs.y += t.y; vs.z += t.z; vs.w += t.w;
+            }
+            const float vv[4] = {vs.x, vs.y, vs.z, vs.w};
+            uint4 bq[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    bq[u][h] = q0 + u < r.rank ? __ldg(reinterpret_cast<const uint4 *>(B + (size_t)(q0 + u) * g.n_feat) + h)
+                                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float vq = q0 + u < r.rank ? vv[u] : 0.f;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&bq[u][h]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(b2[e]);
+                        v[h * 8 + 2 * e] = fmaf(vq, f.x, v[h * 8 + 2 * e]);
+                        v[h * 8 + 2 * e + 1] = fmaf(vq, f.y, v[h * 8 + 2 * e + 1]);
+                    }
+                }
+            }
+        }
     }
     if (g.out_f32) {
         float *o = reinterpret_cast<float *>(g.out) + (size_t)r.out_row * g.ld_out + j0;
@@ -354,6 +429,16 @@ __device__ __forceinline__ void emit8(const GemmArgs &g, const TokMeta &m, const
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier of the 128 epilogue threads that also returns whether v held on all of them
+__device__ __forceinline__ bool vs_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
 
 template <int BN, bool TF32>
 __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
@@ -367,8 +452,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const int stages = g.stages;
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + stages * STAGE_BYTES);
+    // tokens on P with an owned low-rank term (bf16): its expand runs on the
+    // tensor cores as one extra K block per tile, from operands the epilogue
+    // warps write after the ring: A (128 rows x 64 bytes), then B (BN rows)
+    const bool lr_fused = g.tok_on_p && g.v != nullptr;
+    uint8_t *lr_buf = smem + stages * STAGE_BYTES;
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(lr_buf + (lr_fused ? LR_A_BYTES + BN * 64 : 0));
     TokMeta *tmeta = reinterpret_cast<TokMeta *>(reinterpret_cast<uint8_t *>(ctrl) + CTRL_BYTES);
+    // features on P: per-token metadata, then the tokens' v
     float *vtile = reinterpret_cast<float *>(tmeta + BN);
     volatile int *abort_flag = &ctrl->abort;
 
@@ -405,7 +496,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             ptx::mbar_init(ptx::smem_u32(&ctrl->tempty[a]), 4);
         }
         ptx::mbar_init(ptx::smem_u32(&ctrl->drain), 1);
+        ptx::mbar_init(ptx::smem_u32(&ctrl->lrfull), 128);
         ctrl->abort = 0;
+        for (int p = 0; p < 2; ++p) {
+            ctrl->lr_steps[p] = 0;
+            for (int j = 0; j < LR_KSTEPS; ++j) ctrl->lr_aid[p][j] = -2;
+        }
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&g.mapP);
         ptx::prefetch_tmap(&g.mapQ);
@@ -498,6 +594,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            uint32_t lr_par = 0;
             for (int tile = tile0; tile < n_tiles; tile += tstep) {
                 if (!wait_bar(ptx::smem_u32(&ctrl->tempty[acc]), acc_phase ^ 1, abort_flag)) goto mma_done;
                 ptx::tc_fence_after();
@@ -523,6 +620,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                     }
                     ptx::mma_commit(ptx::smem_u32(&ctrl->empty[stage]));
                     if (++stage == stages) { stage = 0; phase ^= 1; }
+                }
+                if (lr_fused) {
+                    // the owned low-rank expand of this tile, into the same
+                    // accumulator (its rows are added before s is applied)
+                    if (!wait_bar(ptx::smem_u32(&ctrl->lrfull), lr_par, abort_flag)) goto mma_done;
+                    ptx::tc_fence_after();
+                    const int steps = ctrl->lr_steps[lr_par];
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                    const uint64_t da = sw64_desc(ptx::smem_u32(lr_buf));
+                    const uint64_t db = sw64_desc(ptx::smem_u32(lr_buf + LR_A_BYTES));
+                    for (int j = 0; j < steps && j < LR_KSTEPS; ++j)
+                        ptx::mma_bf16(d_tmem, da + 2 * j, db + 2 * j, IDESC, 1u);
+                    lr_par ^= 1u;
                 }
                 ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
@@ -575,10 +685,140 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
         }
         int acc = 0;
         uint32_t acc_phase = 0;
+        // tokens on P with an owned low-rank term: before each tile's
+        // accumulator wait, the epilogue warps write that tile's low-rank
+        // operands (the buffer is free: the previous tile's accumulator, which
+        // includes its low-rank MMAs, is complete)
+        const uint32_t lrfull = ptx::smem_u32(&ctrl->lrfull);
+        uint32_t lr_par = 0;
+        bool ok = true;            // this thread's wait of the previous tile succeeded
         for (int tile = tile0; tile < n_tiles; tile += tstep) {
-            if (!wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag)) break;
-            ptx::tc_fence_after();
             const int ft = tile % g.n_ft, tt = tile / g.n_ft;
+            int i = 0;
+            bool live = false;
+            TokMeta rc;
+            const float *vsrc = nullptr;
+            if (lr_fused) {
+                const int par = (int)lr_par;
+                i = tt * TILE_M + row;
+                live = i < n_tok;
+                int a = -1, prev = -2;
+                if (live) {
+                    rc = tok_meta(g, i, sorted_base);
+                    a = g.aid_s[sorted_base + i];
+                    if (row > 0) prev = g.aid_s[sorted_base + i - 1];
+                }
+                const bool own = live && rc.B != nullptr;
+                const bool mma_ok = own && rc.Bm != nullptr && rc.rank <= 16 * LR_KSTEPS;
+                // k-steps in row order: the first row of each adapter in the
+                // tile asks for ceil(rank / 16) of them
+                const int need = (mma_ok && prev != a) ? (rc.rank + 15) / 16 : 0;
+                int incl = need;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                if (lane == 31) ctrl->lr_wsum[par][q] = incl;
+                // every thread is done with the previous tile, and every wait
+                // of it succeeded
+                if (!vs_all(ok)) break;
+                if (et == 0) {
+                    ctrl->lr_steps[par ^ 1] = 0;
+                    for (int j = 0; j < LR_KSTEPS; ++j) ctrl->lr_aid[par ^ 1][j] = -2;
+                }
+                if (need > 0) {
+                    int k0 = incl - need;
+                    for (int w = 0; w < q; ++w) k0 += ctrl->lr_wsum[par][w];
+                    if (k0 + need <= LR_KSTEPS) {
+                        for (int j = k0; j < k0 + need; ++j) {
+                            ctrl->lr_aid[par][j] = a;
+                            ctrl->lr_k0[par][j] = k0;
+                            ctrl->lr_rank[par][j] = rc.rank;
+                            ctrl->lr_B[par][j] = rc.Bm;
+                        }
+                        atomicMax(&ctrl->lr_steps[par], k0 + need);
+                    }
+                }
+                epi_bar();   // the tile's k-steps are assigned
+                int k0 = -1;
+                if (mma_ok)
+                    for (int j = 0; j < LR_KSTEPS; ++j)
+                        if (ctrl->lr_aid[par][j] == a) { k0 = j; break; }
+                if (own && k0 < 0) vsrc = g.v + (size_t)(sorted_base + i) * g.v_ld;
+                // A: this row's v (summed over the K chunks in chunk order,
+                // rounded to bf16) in its adapter's k-steps, zeros elsewhere
+                {
+                    float vv[16 * LR_KSTEPS];
+#pragma unroll
+                    for (int c = 0; c < 16 * LR_KSTEPS; ++c) vv[c] = 0.f;
+                    if (k0 >= 0) {
+                        const float *src = g.v + (size_t)(sorted_base + i) * g.v_ld;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4 * LR_KSTEPS; ++c4) {
+                            const int qq = 4 * c4 - 16 * k0;
+                            if (qq >= 0 && qq < rc.rank) {
+                                float4 sum = __ldg(reinterpret_cast<const float4 *>(src + qq));
+                                for (int s = 1; s < g.v_ks; ++s) {
+                                    const float4 t = __ldg(reinterpret_cast<const float4 *>(src + s * g.v_kstride + qq));
+                                    sum.x += t.x; sum.y += t.y; sum.z += t.z; sum.w += t.w;
+                                }
+                                vv[4 * c4] = sum.x;
+                                vv[4 * c4 + 1] = qq + 1 < rc.rank ? sum.y : 0.f;
+                                vv[4 * c4 + 2] = qq + 2 < rc.rank ? sum.z : 0.f;
+                                vv[4 * c4 + 3] = qq + 3 < rc.rank ? sum.w : 0.f;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2 * LR_KSTEPS; ++u) {
+                        uint4 pk;
+                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(vv[8 * u + 2 * e], vv[8 * u + 2 * e + 1]);
+                        *reinterpret_cast<uint4 *>(lr_buf + sw64_offset(row, u)) = pk;
+                    }
+                }
+                // B: for features n of this tile, each k-step's 16 rank rows of
+                // its adapter's B at column n (zeros past the rank, past the
+                // features, and in k-steps no adapter took)
+                for (int n = et; n < BN; n += 128) {
+                    const int col = ft * BN + n;
+#pragma unroll
+                    for (int j = 0; j < LR_KSTEPS; ++j) {
+                        const int aj = ctrl->lr_aid[par][j];
+                        float bv[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) bv[e] = 0.f;
+                        if (aj != -2 && col < g.n_feat) {
+                            const __nv_bfloat16 *Bj = reinterpret_cast<const __nv_bfloat16 *>(ctrl->lr_B[par][j]);
+                            const int q0 = 16 * (j - ctrl->lr_k0[par][j]);
+                            const int rk = ctrl->lr_rank[par][j];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                if (q0 + e < rk) bv[e] = __bfloat162float(Bj[(size_t)(q0 + e) * g.n_feat + col]);
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint4 pk;
+                            __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(bv[8 * h + 2 * e], bv[8 * h + 2 * e + 1]);
+                            *reinterpret_cast<uint4 *>(lr_buf + LR_A_BYTES + sw64_offset(n, 2 * j + h)) = pk;
+                        }
+                    }
+                }
+                // generic-proxy writes made visible to the tensor cores, then
+                // the MMA issuer may read them
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                ptx::mbar_arrive(lrfull);
+                lr_par ^= 1u;
+                ok = wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag);
+                if (!ok) continue;   // every thread learns of it at the next tile's vote
+            } else {
+                if (!wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag)) break;
+            }
+            ptx::tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const uint32_t tbv = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)BN;
             if (!g.tok_on_p) {
@@ -604,10 +844,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                 }
             } else {
                 // tokens on rows, features on columns
-                const int i = tt * TILE_M + row;
-                const bool live = i < n_tok;
-                TokMeta rc;
-                if (live) rc = tok_meta(g, i, sorted_base);
+                if (!lr_fused) {
+                    i = tt * TILE_M + row;
+                    live = i < n_tok;
+                    if (live) rc = tok_meta(g, i, sorted_base);
+                }
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
@@ -618,7 +859,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[acc]));
                     }
                     const int j0 = ft * BN + c * 32;
-                    if (live && j0 < g.n_feat) emit32(g, rc, j0, v);
+                    if (live && j0 < g.n_feat) emit32(g, rc, j0, v, vsrc);
                 }
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
@@ -748,10 +989,13 @@ cudaError_t launch_one(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bo
 
 }  // namespace
 
-size_t gemm_smem_bytes(int bn, int stages, int lr_rmax) {
+// Dynamic shared memory of one launch.  Tokens on P with an owned low-rank
+// term (lr_rmax > 0): the tensor-core expand's operands follow the ring.
+size_t gemm_smem_bytes(int bn, int stages, int lr_rmax, bool tok_on_p) {
     const size_t stage_bytes = (size_t)TILE_M * 128 + (size_t)bn * 128;
-    return 1024 + (size_t)stages * stage_bytes + CTRL_BYTES + (size_t)bn * sizeof(TokMeta) +
-           (size_t)bn * lr_rmax * sizeof(float);
+    const size_t epi = tok_on_p ? (lr_rmax > 0 ? (size_t)LR_A_BYTES + (size_t)bn * 64 : 0)
+                                : (size_t)bn * sizeof(TokMeta) + (size_t)bn * lr_rmax * sizeof(float);
+    return 1024 + (size_t)stages * stage_bytes + CTRL_BYTES + epi;
 }
 
 GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms, int lr_rmax) {
@@ -764,6 +1008,7 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         p.bn = n_feat <= 256 ? 64 : 256;
         p.splits = 1;
         p.stages = 4;
+        while (p.stages > 2 && gemm_smem_bytes(p.bn, p.stages, lr_rmax, true) > GEMM_SMEM_MAX) --p.stages;
         const int tiles = ((n_tok + TILE_M - 1) / TILE_M) * ((n_feat + p.bn - 1) / p.bn);
         p.grid = tiles < num_sms ? tiles : num_sms;
     } else {
@@ -776,7 +1021,7 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         const int target = per_sm * num_sms;
         p.stages = p.bn == 64 ? 4 : (p.bn == 128 ? 5 : 4);
         // two CTAs of the 64-token tile share an SM: keep both within its shared memory
-        while (p.bn == 64 && p.stages > 2 && 2 * (gemm_smem_bytes(p.bn, p.stages, lr_rmax) + 1024) > 228 * 1024)
+        while (p.bn == 64 && p.stages > 2 && 2 * (gemm_smem_bytes(p.bn, p.stages, lr_rmax, false) + 1024) > 228 * 1024)
             --p.stages;
         int s = 1;
         while (s < 8 && tiles * (s * 2) <= target && kblocks / (s * 2) >= 4) s *= 2;
@@ -784,7 +1029,7 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         p.grid = tiles * s;
     }
     if (p.grid < 1) p.grid = 1;
-    p.smem = gemm_smem_bytes(p.bn, p.stages, lr_rmax);
+    p.smem = gemm_smem_bytes(p.bn, p.stages, lr_rmax, tok_on_p);
     return p;
 }
 

@@ -386,7 +386,7 @@ template <typename T, int RM>
 cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int *perm, const int *seg_start,
                       const int *seg_aid, const int *seg_unit, const IndexMeta *meta, const Slot *slots,
                       float *v_part, int max_tokens, void *out, int out_f32, cudaStream_t st, bool pdl,
-                      bool shrink) {
+                      bool shrink, bool expand) {
     int kchunk = 0;
     const int ks = lowrank_ks(d_in, &kchunk);
     cudaLaunchAttribute attr;
@@ -408,6 +408,7 @@ cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int
                                v_part, max_tokens, kchunk);
         if (e != cudaSuccess) return e;
     }
+    if (!expand) return cudaSuccess;
     cfg.dynamicSmemBytes = 0;
     cfg.gridDim = dim3((unsigned)unit_bound, (unsigned)((d_out + 2047) / 2048), 1);
     if (sizeof(T) == 2 && RM == 16 && !out_f32)
@@ -422,20 +423,20 @@ cudaError_t launch_lr(const T *x, int d_in, int d_out, int unit_bound, const int
 cudaError_t launch_lowrank(bool f32, const void *x, int d_in, int d_out, int unit_bound, const int *perm,
                            const int *seg_start, const int *seg_aid, const int *seg_unit,
                            const IndexMeta *meta, const Slot *slots, float *v_part, int max_tokens, void *out,
-                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink) {
+                           int out_f32, cudaStream_t st, bool pdl, int max_rank, bool shrink, bool expand) {
     if (f32) {
         if (max_rank <= 16)
             return launch_lr<float, 16>((const float *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid, seg_unit,
-                                        meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
+                                        meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink, expand);
         return launch_lr<float, 64>((const float *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid, seg_unit,
-                                    meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
+                                    meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink, expand);
     }
     if (max_rank <= 16)
         return launch_lr<__nv_bfloat16, 16>((const __nv_bfloat16 *)x, d_in, d_out, unit_bound, perm, seg_start,
                                             seg_aid, seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl,
-                                            shrink);
+                                            shrink, expand);
     return launch_lr<__nv_bfloat16, 64>((const __nv_bfloat16 *)x, d_in, d_out, unit_bound, perm, seg_start, seg_aid,
-                                        seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink);
+                                        seg_unit, meta, slots, v_part, max_tokens, out, out_f32, st, pdl, shrink, expand);
 }
 
 }  // namespace scute

@@ -93,23 +93,37 @@ def _layer_counts(ids, adapters: dict, d_in: int, d_out: int, shared_rank: int, 
     return c
 
 
-def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool) -> list:
-    """Launches of one layer's call on the per-kernel plan, (name, bytes, flops)."""
+def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool, lr_fused: bool = False) -> list:
+    """Launches of one layer's call on the per-kernel plan, (name, bytes, flops).
+
+    With ``lr_fused`` (bf16 contexts, more than 256 tokens) the owned shrink
+    runs before the base GEMM and the owned expand inside the GEMM's epilogue:
+    the GEMM then also reads the shrink's partial v and each B', and out is
+    written once."""
     n, E, Eo, kd, d_in, d_out = c["n"], c["E"], c["Eo"], c["kd"], c["d_in"], c["d_out"]
     rv, krv = c["rv"], c["krv"]
     index_out = 8 * n + 4 * (c["segments"] + 1) + 4 * c["segments"] + 88
+    ks = lowrank_ks(d_in)
+    shrink = ("lr_shrink", c["n_lr"] * d_in * E + c["A_b"] + ks * c["lr_rank_rows"] * 4,
+              2 * c["lr_rank_rows"] * d_in)
+    fused = lowrank_launched and lr_fused
+    # W, x', s/b vectors, perm/ids, out (and the fused expand's v partials and B')
+    gemm_b = d_out * kd * E + n * kd * E + c["sb_b"] + 8 * n + n * d_out * Eo
+    gemm_f = 2 * n * kd * d_out
+    if fused:
+        gemm_b += ks * c["lr_rank_rows"] * 4 + c["B_b"]
+        gemm_f += 2 * c["lr_rank_rows"] * d_out
     kernels = [
         # ids in; perm and sorted ids out; segment table; 22-int summary
         ("index", 4 * n + index_out, 0),
         # x in, perm/ids in, R of each distinct rotating adapter, x' out
         ("rotate", n * d_in * E + 8 * n + c["R_b"] + n * kd * E, 2 * c["n_rot"] * d_in * 32),
-        # W, x', s/b vectors, perm/ids, out
-        ("base_gemm", d_out * kd * E + n * kd * E + c["sb_b"] + 8 * n + n * d_out * Eo, 2 * n * kd * d_out),
     ]
-    if lowrank_launched:
-        ks = lowrank_ks(d_in)
-        kernels.append(("lr_shrink", c["n_lr"] * d_in * E + c["A_b"] + ks * c["lr_rank_rows"] * 4,
-                        2 * c["lr_rank_rows"] * d_in))
+    if fused:
+        kernels.append(shrink)
+    kernels.append(("base_gemm", gemm_b, gemm_f))
+    if lowrank_launched and not fused:
+        kernels.append(shrink)
         kernels.append(("lr_expand", ks * c["lr_rank_rows"] * 4 + c["B_b"] + 2 * c["n_lr"] * d_out * Eo,
                         2 * c["lr_rank_rows"] * d_out))
     if vera_launched:
@@ -155,7 +169,8 @@ def batch_bytes(ids, layers: list, dtype: str, out_dtype: str, variant: int = 0)
     else:
         kernels = []
         for L, c in zip(layers, cs):
-            kernels += _per_kernel_plan(c, L["lowrank_launched"], L["vera_launched"])
+            kernels += _per_kernel_plan(c, L["lowrank_launched"], L["vera_launched"],
+                                        lr_fused=dtype != "fp32" and n > 256)
     return {
         "kernels": kernels,
         "algorithmic_bytes": alg,

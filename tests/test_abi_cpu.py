@@ -199,6 +199,37 @@ def test_batch_byte_model_matches_oracle(lib):
             assert abs(t - OBM.predict_time_us(ref["kernels"], bw, tf, lc)) <= 1e-9 * max(1.0, t)
 
 
+def test_fused_expand_plan_moves_only_the_out_rewrite():
+    """bf16 batches above 256 tokens run the owned expand inside the base
+    GEMM's epilogue.  Against the separate expand the launch list loses
+    lr_expand, the shrink comes before the GEMM, the GEMM gains the expand's
+    v partials, B' and flops, and the total bytes drop by exactly the owned
+    rows of out read and written once more; the flops are unchanged."""
+    w = WL.prefill_mixed(n_req=6, lo=40, hi=200, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down"))
+    assert w.n > 256
+    for layer in ("q", "up"):
+        L, ads, lowrank, vera = _bm_inputs(w, layer, "bf16")
+        assert lowrank
+        c = OBM._layer_counts(w.ids, ads, L.d_in, L.d_out, L.shared_rank, "bf16", "bf16")
+        sep = OBM._per_kernel_plan(c, lowrank, vera, lr_fused=False)
+        fus = OBM._per_kernel_plan(c, lowrank, vera, lr_fused=True)
+        names_sep, names_fus = [k[0] for k in sep], [k[0] for k in fus]
+        assert names_sep[:5] == ["index", "rotate", "base_gemm", "lr_shrink", "lr_expand"]
+        assert names_fus[:4] == ["index", "rotate", "lr_shrink", "base_gemm"]
+        assert "lr_expand" not in names_fus and names_fus[4:] == names_sep[5:]
+        ks = OBM.lowrank_ks(L.d_in)
+        g_sep, g_fus = dict((k[0], k) for k in sep)["base_gemm"], dict((k[0], k) for k in fus)["base_gemm"]
+        assert g_fus[1] - g_sep[1] == ks * c["lr_rank_rows"] * 4 + c["B_b"]
+        assert g_fus[2] - g_sep[2] == 2 * c["lr_rank_rows"] * L.d_out
+        assert sum(k[1] for k in sep) - sum(k[1] for k in fus) == 2 * c["n_lr"] * L.d_out * 2
+        assert sum(k[2] for k in sep) == sum(k[2] for k in fus)
+        # the public entry takes the fused plan for bf16 above 256 tokens only
+        ref = OBM.call_bytes(w.ids, ads, L.d_in, L.d_out, L.shared_rank, "bf16", "bf16", lowrank, vera)
+        assert [k[0] for k in ref["kernels"]] == names_fus
+        ref = OBM.call_bytes(w.ids[:256], ads, L.d_in, L.d_out, L.shared_rank, "bf16", "bf16", lowrank, vera)
+        assert "lr_expand" in [k[0] for k in ref["kernels"]]
+
+
 def test_time_model_hand_example(lib):
     """Two launches counted by hand: 1e6 bytes at 1000 GB/s is 1 us; 2e9 flops
     at 1000 TFLOP/s is 2 us, so the first launch takes max(1, 2) = 2 us; the
