@@ -76,11 +76,14 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
     }
     __syncthreads();
     int tot = 0;
-    if (tid < 256)
+    if (tid < 256) {
+#pragma unroll 8
         for (int k = 0; k < nw; ++k) tot += hist[k * 256 + tid];
+    }
     const int excl = block_excl_scan(tid < 256 ? tot : 0, s_warp, nullptr);
     if (tid < 256) {
         int run = excl;
+#pragma unroll 8
         for (int k = 0; k < nw; ++k) {
             const int c = hist[k * 256 + tid];
             hist[k * 256 + tid] = run;
@@ -154,18 +157,21 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     radix_pass(bufA, bufB, n, 16, hist, s_warp);
     radix_pass(bufB, bufA, n, 24, hist, s_warp);
 
-    // segments: runs of one key; each thread owns a contiguous run of rows
-    const int per = (n + blockDim.x - 1) / blockDim.x;
-    const int r0 = min(n, tid * per), r1 = min(n, r0 + per);
-    int nflag = 0;
-    for (int i = r0; i < r1; ++i) {
+    // the per-row outputs, with consecutive threads on consecutive rows (one
+    // SM writes them all: a strided pattern would cost a store sector per row)
+    for (int i = tid; i < n; i += blockDim.x) {
         const uint32_t v = bufA[i];
         const uint32_t key = v >> 16;
         const int rank = (int)(key / (uint32_t)A);
         perm[i] = (int)(v & 0xFFFFu);
         aid_s[i] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
-        if (i == 0 || (bufA[i - 1] >> 16) != key) ++nflag;
     }
+    // segments: runs of one key; each thread owns a contiguous run of rows
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int r0 = min(n, tid * per), r1 = min(n, r0 + per);
+    int nflag = 0;
+    for (int i = r0; i < r1; ++i)
+        if (i == 0 || (bufA[i - 1] >> 16) != (bufA[i] >> 16)) ++nflag;
     int total = 0;
     int s = block_excl_scan(nflag, s_warp, &total);
     for (int i = r0; i < r1; ++i) {
