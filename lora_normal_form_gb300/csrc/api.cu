@@ -1126,7 +1126,8 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         e.out = out;
         e.out_f32 = out_f32;
         e.ld_out = L.d_out;
-        GemmPlan pe = plan_gemm(nn, L.d_out, e.kblocks, tok_on_p, f32, c->num_sms);
+        e.stage_out = tok_on_p && !f32 && !out_f32 ? 1 : 0;
+        GemmPlan pe = plan_gemm(nn, L.d_out, e.kblocks, tok_on_p, f32, c->num_sms, 0, e.stage_out != 0);
         e.splits = pe.splits;
         e.stages = pe.stages;
         e.part = c->gpart;

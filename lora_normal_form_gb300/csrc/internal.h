@@ -89,6 +89,9 @@ struct GemmArgs {
     int *status;
     // fused epilogue
     int vera_kb;               // VeRA expand K blocks folded into this GEMM (0 = none; features on P)
+    int stage_out;             // EPI_VERA_E, tokens on P, bf16 out: each tile's rows of out are
+                               // read into shared memory before its accumulator is complete
+                               // and written back with coalesced stores
     // owned low-rank intermediate (null = none).  Features on P: v[row * v_ld + q].
     // Tokens on P (bf16): the K-chunk partials of the shrink, summed in chunk
     // order, v[s * v_kstride + row * v_ld + q] for s < v_ks; the expand runs as
@@ -127,7 +130,7 @@ struct GemmPlan {
 };
 
 GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms,
-                   int lr_rmax = 0);
+                   int lr_rmax = 0, bool stage_out = false);
 cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl);
 
 // K splits of the owned low-rank shrink: chunks of about 2048 elements, at

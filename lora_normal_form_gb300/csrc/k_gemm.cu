@@ -90,6 +90,10 @@ __host__ __device__ constexpr uint32_t instr_desc(bool tf32, int M, int N) {
 // extra K block of LR_KSTEPS x 16 columns, A = the rows' v (each row in the
 // columns of its adapter's k-steps, zeros elsewhere), B = the tile's features
 // of each adapter's B, both K-major in the 64-byte-swizzle layout.
+// bytes between rows of a tile's staged bf16 output (the 16 extra bytes put
+// the rows read by one quarter-warp in different banks)
+__host__ __device__ constexpr int out_pitch(int bn) { return bn * 2 + 16; }
+
 constexpr int LR_KSTEPS = 2;
 constexpr int LR_A_BYTES = TILE_M * 64;
 
@@ -440,7 +444,9 @@ __device__ __forceinline__ bool vs_all(bool v) {
     return r != 0;
 }
 
-template <int BN, bool TF32>
+// SO: the VeRA expand with its rows of out staged in shared memory (tokens on
+// P, bf16; a separate instance, so that the other launches' code is unchanged)
+template <int BN, bool TF32, bool SO>
 __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     gemm_tc_kernel(const __grid_constant__ GemmArgs g) {
     constexpr int STAGE_BYTES = TILE_M * 128 + BN * 128;
@@ -691,6 +697,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
         // includes its low-rank MMAs, is complete)
         const uint32_t lrfull = ptx::smem_u32(&ctrl->lrfull);
         uint32_t lr_par = 0;
+        // VeRA expand, tokens on P, bf16 out: staged rows of out and e slices
+        constexpr bool stage_out = SO && !TF32;
+        uint8_t *obuf = reinterpret_cast<uint8_t *>(ctrl) + CTRL_BYTES;
+        float *ebuf = reinterpret_cast<float *>(obuf + TILE_M * out_pitch(BN));
+        const float *ew = nullptr;
         bool ok = true;            // this thread's wait of the previous tile succeeded
         for (int tile = tile0; tile < n_tiles; tile += tstep) {
             const int ft = tile % g.n_ft, tt = tile / g.n_ft;
@@ -815,6 +826,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                 lr_par ^= 1u;
                 ok = wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag);
                 if (!ok) continue;   // every thread learns of it at the next tile's vote
+            } else if (stage_out) {
+                // this warp's 32 rows of out at the tile's features, and the
+                // e slice of its first row's adapter, copied to shared memory
+                // while the accumulator forms (one row per warp instruction)
+                i = tt * TILE_M + row;
+                live = i < n_tok;
+                if (live) rc = tok_meta(g, i, sorted_base);
+                const int cols = min(BN, g.n_feat - ft * BN);
+                const long long my_orow = live ? rc.out_row : 0;
+                for (int r = 0; r < 32; ++r) {
+                    const long long orow_r = __shfl_sync(0xffffffffu, my_orow, r);
+                    const int live_r = __shfl_sync(0xffffffffu, live ? 1 : 0, r);
+                    if (live_r && lane * 16 < cols * 2)
+                        ptx::cp_async16(ptx::smem_u32(obuf + (q * 32 + r) * out_pitch(BN) + lane * 16),
+                                        reinterpret_cast<const __nv_bfloat16 *>(g.out) + orow_r * g.ld_out +
+                                            (size_t)ft * BN + lane * 8);
+                }
+                ew = reinterpret_cast<const float *>(__shfl_sync(
+                    0xffffffffu, (unsigned long long)(live ? rc.v1 : nullptr), 0));
+                if (ew)
+                    for (int k = lane; k * 4 < cols; k += 32)
+                        ptx::cp_async16(ptx::smem_u32(ebuf + q * BN + 4 * k), ew + (size_t)ft * BN + 4 * k);
+                ptx::cp_async_commit();
+                if (!wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag)) break;
+                ptx::cp_async_wait_all();
+                __syncwarp();
             } else {
                 if (!wait_bar(ptx::smem_u32(&ctrl->tfull[acc]), acc_phase, abort_flag)) break;
             }
@@ -842,6 +879,69 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
                         for (int k = 0; k < 32; ++k) redv[(c * 32 + k) * ld + row] = v[k];
                     }
                 }
+            } else if (stage_out) {
+                // out += acc * e on the staged rows, then the warp writes its
+                // 32 rows back, one row per instruction
+                const int cols = min(BN, g.n_feat - ft * BN);
+                uint8_t *orow = obuf + row * out_pitch(BN);
+                const bool e_sh = live && rc.v1 != nullptr && rc.v1 == ew;
+                // y = acc * e + old for 32 features [32c, 32c + 32) of this row
+                auto add_chunk = [&](int c, const float (&v)[32]) {
+                    if (!live || c * 32 >= cols) return;
+                    const float *ep = e_sh ? ebuf + q * BN + c * 32
+                                           : (rc.v1 ? rc.v1 + (size_t)ft * BN + c * 32 : nullptr);
+                    uint4 *op = reinterpret_cast<uint4 *>(orow + c * 64);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        float e8[8];
+                        if (ep) {
+                            const float4 a0 = e_sh ? reinterpret_cast<const float4 *>(ep)[2 * h]
+                                                   : __ldg(reinterpret_cast<const float4 *>(ep) + 2 * h);
+                            const float4 a1 = e_sh ? reinterpret_cast<const float4 *>(ep)[2 * h + 1]
+                                                   : __ldg(reinterpret_cast<const float4 *>(ep) + 2 * h + 1);
+                            e8[0] = a0.x; e8[1] = a0.y; e8[2] = a0.z; e8[3] = a0.w;
+                            e8[4] = a1.x; e8[5] = a1.y; e8[6] = a1.z; e8[7] = a1.w;
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) e8[k] = 1.f;
+                        }
+                        const uint4 prev = op[h];
+                        const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&prev);
+                        uint4 pk;
+                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(q2[e]);
+                            p2[e] = __floats2bfloat162_rn(v[8 * h + 2 * e] * e8[2 * e] + f.x,
+                                                          v[8 * h + 2 * e + 1] * e8[2 * e + 1] + f.y);
+                        }
+                        op[h] = pk;
+                    }
+                };
+                // two accumulator chunks in flight per wait
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    float v0[32], v1[32];
+                    ptx::tmem_ld32x2(tb + c * 32, tb + (c + 1) * 32, v0, v1);
+                    if (c + 2 == BN / 32) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&ctrl->tempty[acc]));
+                    }
+                    add_chunk(c, v0);
+                    add_chunk(c + 1, v1);
+                }
+                __syncwarp();
+                const long long my_orow = live ? rc.out_row : 0;
+                for (int r = 0; r < 32; ++r) {
+                    const long long orow_r = __shfl_sync(0xffffffffu, my_orow, r);
+                    const int live_r = __shfl_sync(0xffffffffu, live ? 1 : 0, r);
+                    if (live_r && lane * 16 < cols * 2)
+                        *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(g.out) + orow_r * g.ld_out +
+                                                   (size_t)ft * BN + lane * 8) =
+                            *reinterpret_cast<const uint4 *>(obuf + (q * 32 + r) * out_pitch(BN) + lane * 16);
+                }
+                __syncwarp();   // the rows are read before the next tile's copies land
             } else {
                 // tokens on rows, features on columns
                 if (!lr_fused) {
@@ -864,6 +964,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (stage_out) ptx::cp_async_wait_all();   // no copy in flight at exit
     }
 
     ptx::tc_fence_before();
@@ -955,10 +1056,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, BN == 64 ? 2 : 1)
     if (!g.tok_on_p && splits > 1) ptx::cluster_wait();
 }
 
-template <int BN, bool TF32>
+template <int BN, bool TF32, bool SO = false>
 cudaError_t launch_one(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl) {
     static std::atomic<unsigned long long> attr_done{0};
-    auto kern = gemm_tc_kernel<BN, TF32>;
+    auto kern = gemm_tc_kernel<BN, TF32, SO>;
     {
         const cudaError_t e = allow_max_dynamic_smem(kern, attr_done);
         if (e != cudaSuccess) return e;
@@ -991,14 +1092,16 @@ cudaError_t launch_one(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bo
 
 // Dynamic shared memory of one launch.  Tokens on P with an owned low-rank
 // term (lr_rmax > 0): the tensor-core expand's operands follow the ring.
-size_t gemm_smem_bytes(int bn, int stages, int lr_rmax, bool tok_on_p) {
+size_t gemm_smem_bytes(int bn, int stages, int lr_rmax, bool tok_on_p, bool stage_out = false) {
     const size_t stage_bytes = (size_t)TILE_M * 128 + (size_t)bn * 128;
     const size_t epi = tok_on_p ? (lr_rmax > 0 ? (size_t)LR_A_BYTES + (size_t)bn * 64 : 0)
                                 : (size_t)bn * sizeof(TokMeta) + (size_t)bn * lr_rmax * sizeof(float);
-    return 1024 + (size_t)stages * stage_bytes + CTRL_BYTES + epi;
+    const size_t so = stage_out ? (size_t)TILE_M * out_pitch(bn) + (size_t)4 * bn * sizeof(float) : 0;
+    return 1024 + (size_t)stages * stage_bytes + CTRL_BYTES + epi + so;
 }
 
-GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms, int lr_rmax) {
+GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32, int num_sms, int lr_rmax,
+                   bool stage_out) {
     GemmPlan p{};
     p.tf32 = tf32 ? 1 : 0;
     if (tok_on_p) {
@@ -1008,7 +1111,7 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         p.bn = n_feat <= 256 ? 64 : 256;
         p.splits = 1;
         p.stages = 4;
-        while (p.stages > 2 && gemm_smem_bytes(p.bn, p.stages, lr_rmax, true) > GEMM_SMEM_MAX) --p.stages;
+        while (p.stages > 2 && gemm_smem_bytes(p.bn, p.stages, lr_rmax, true, stage_out) > GEMM_SMEM_MAX) --p.stages;
         const int tiles = ((n_tok + TILE_M - 1) / TILE_M) * ((n_feat + p.bn - 1) / p.bn);
         p.grid = tiles < num_sms ? tiles : num_sms;
     } else {
@@ -1029,11 +1132,14 @@ GemmPlan plan_gemm(int n_tok, int n_feat, int kblocks, bool tok_on_p, bool tf32,
         p.grid = tiles * s;
     }
     if (p.grid < 1) p.grid = 1;
-    p.smem = gemm_smem_bytes(p.bn, p.stages, lr_rmax, tok_on_p);
+    p.smem = gemm_smem_bytes(p.bn, p.stages, lr_rmax, tok_on_p, tok_on_p && stage_out);
     return p;
 }
 
 cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, bool pdl) {
+    // the staged-output instance (its shared memory is in the plan) for the
+    // VeRA expand of bf16 outputs with tokens on P
+    const bool so = g.stage_out && g.tok_on_p && g.epi == EPI_VERA_E && !g.out_f32;
     if (p.tf32) {
         switch (p.bn) {
             case 64: return launch_one<64, true>(g, p, st, pdl);
@@ -1042,9 +1148,9 @@ cudaError_t launch_gemm(const GemmArgs &g, const GemmPlan &p, cudaStream_t st, b
         }
     }
     switch (p.bn) {
-        case 64: return launch_one<64, false>(g, p, st, pdl);
+        case 64: return so ? launch_one<64, false, true>(g, p, st, pdl) : launch_one<64, false>(g, p, st, pdl);
         case 128: return launch_one<128, false>(g, p, st, pdl);
-        default: return launch_one<256, false>(g, p, st, pdl);
+        default: return so ? launch_one<256, false, true>(g, p, st, pdl) : launch_one<256, false>(g, p, st, pdl);
     }
 }
 
