@@ -297,6 +297,25 @@ def test_small_prefill_parity(scute, out_dtype):
     ctx.close()
 
 
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_prefill_more_tiles_than_sms(scute, out_dtype):
+    """About 4000 tokens on the ragged small shapes: the q and up base GEMMs
+    have more tiles than SMs (160 and 192 for 152), so persistent CTAs run a
+    second, short wave; every row graded, with LoRA / DoRA terms on the
+    tensor-core expand and NF adapters on the CUDA-core one."""
+    w = WL.with_nf_adapters(WL.prefill_mixed(n_req=20, lo=150, hi=250, shapes=WL.SMALL_PROJ, proj=SMALL_NAMES))
+    n = w.n
+    for name in ("q", "up"):
+        tiles = -(-n // 128) * -(-WL.SMALL_PROJ[name][1] // 256)
+        assert tiles >= 152 and 0 < tiles % 152 <= 76, (name, tiles)
+    ctx = H.make_ctx(scute, w)
+    outs = H.run_layers(ctx, w, SMALL_NAMES, out_dtype)
+    assert ctx.sync_status() == 0
+    for name in SMALL_NAMES:
+        H.grade(w, name, outs[name], out_dtype)
+    ctx.close()
+
+
 @pytest.mark.parametrize("rank", [1, 8, 24, 64])
 @pytest.mark.parametrize("n", [200, 700])
 def test_tensor_core_shrink_ranks(scute, rank, n):
