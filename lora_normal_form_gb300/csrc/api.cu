@@ -789,14 +789,52 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
                 t_vs += b1 - b0;
             }
     }
-    // stream-K ranges: every CTA gets about (main + VeRA-shrink blocks) / G,
-    // its VeRA unit counted against its share of main blocks
-    const long long W = blk + t_vs;
+    {
+        // low-rank items are dealt with the calls of most work per item
+        // (d_in + d_out) first, ties in call order
+        unsigned used = 0;
+        for (int o = 0; o < nc; ++o) {
+            int best = 0, bw = -1;
+            for (int i = 0; i < nc; ++i) {
+                const int w = a.call[i].d_in + a.call[i].d_out;
+                if (!((used >> i) & 1u) && w > bw) {
+                    bw = w;
+                    best = i;
+                }
+            }
+            used |= 1u << best;
+            a.it_call[o] = best;
+            a.it_ng[o] = (a.call[best].lr_rmax + 7) / 8;
+        }
+    }
+    // Each CTA's epilogue warps run the low-rank items dealt to it (item it to
+    // CTA G - 1 - it mod G) while its stream runs, and they slow that stream:
+    // an item is charged (d_in + d_out) / ITEM_FEATURES_PER_BLOCK stream blocks
+    // against its CTA, counted on the host's bound of items per call (the
+    // batch's own count is known only on the device).  Per-CTA timestamps on
+    // the 64-token mixed batch: an item delays its CTA by about a third of its
+    // own time; a gate or up item then weighs about 16 blocks.
+    std::vector<long long> icost((size_t)G, 0);
+    {
+        long long it = 0;
+        for (int o = 0; o < nc; ++o) {
+            const StepCall &k = a.call[a.it_call[o]];
+            const long long pen = (long long)(k.d_in + k.d_out) / ITEM_FEATURES_PER_BLOCK;
+            for (int j = 0; j < k.lr_items; ++j, ++it) icost[(size_t)(G - 1 - (int)(it % G))] += pen;
+        }
+    }
+    long long tcost = 0;
+    for (int i = 0; i < G; ++i) tcost += icost[(size_t)i];
+    // stream-K ranges: every CTA gets about (main + VeRA-shrink blocks + item
+    // charges) / G, its VeRA unit and its items counted against its share of
+    // main blocks
+    const long long W = blk + t_vs + tcost;
     long long vsb = 0;
     bool mono = true;
     for (int i = 0; i <= G; ++i) {
         a.start[i] = (long long)i * W / G - vsb;
         if (i < units) vsb += ublk[i];
+        if (i < G) vsb += icost[(size_t)i];
         if (i > 0 && a.start[i] < a.start[i - 1]) mono = false;
     }
     if (!mono || a.start[0] != 0 || a.start[G] != blk)
@@ -829,24 +867,6 @@ static scute_status step_launch(scute_ctx *c, const scute_call *calls, int nc, c
         return fail(c, SCUTE_ERR_UNSUPPORTED, "partial-tile workspace too small for this batch");
     if (SY_TILE + tile > STEP_SYNC_INTS) return fail(c, SCUTE_ERR_UNSUPPORTED, "too many tiles in one batch");
     a.variant = c->variant;
-    {
-        // low-rank items are dealt with the calls of most work per item
-        // (d_in + d_out) first, ties in call order
-        unsigned used = 0;
-        for (int o = 0; o < nc; ++o) {
-            int best = 0, bw = -1;
-            for (int i = 0; i < nc; ++i) {
-                const int w = a.call[i].d_in + a.call[i].d_out;
-                if (!((used >> i) & 1u) && w > bw) {
-                    bw = w;
-                    best = i;
-                }
-            }
-            used |= 1u << best;
-            a.it_call[o] = best;
-            a.it_ng[o] = (a.call[best].lr_rmax + 7) / 8;
-        }
-    }
     {
         // the plan as launched, for scute_debug_step_plan
         std::vector<int64_t> &P = c->last_plan;

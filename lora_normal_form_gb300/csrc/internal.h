@@ -179,6 +179,8 @@ cudaError_t allow_max_dynamic_smem(K kernel, std::atomic<unsigned long long> &do
 // by the CTA holding each tile's first block.
 constexpr int STEP_MAX_CALLS = 8;
 constexpr int STEP_MAX_TOKENS = 128;
+// stream-block charge of one decode low-rank item: (d_in + d_out) / this
+constexpr int ITEM_FEATURES_PER_BLOCK = 1152;
 constexpr int STEP_MAX_GRID = 190;
 constexpr int STEP_MAX_VTILES = 8;     // VeRA shrink tiles per call (shared rank <= 1024)
 
@@ -235,7 +237,7 @@ struct StepArgs {
     float *part;               // partial tiles: slot * 2 planes * 128 * bn floats
     int *sync;
     long long t_main;          // main K blocks over all calls
-    long long w_total;         // main + VeRA shrink K blocks
+    long long w_total;         // main + VeRA shrink K blocks + low-rank item charges
     int n_units;               // VeRA shrink units (<= grid)
     int vs_ch;                 // K blocks per VeRA shrink unit
     int n_tiles;               // main tiles over all calls

@@ -25,6 +25,7 @@ STEP_MAX_VTILES = 8
 STEP_SYNC_INTS = 1 << 16
 SY_XS, SY_LR, SY_U, SY_EXIT, SY_ABORT, SY_VTILE, SY_TILE = 0, 8, 16, 24, 25, 32, 96
 MAX_RANK = 64
+ITEM_FEATURES_PER_BLOCK = 1152
 TILE_M = 128
 BOX_ROWS = 64
 EPI_THREADS = 256
@@ -168,12 +169,27 @@ def plan(layers: Sequence[LayerShape], n: int, grid: int, ws: Dict[str, int],
                 ublk.append(b1 - b0)
                 t_vs += b1 - b0
                 u += 1
-    W = blk + t_vs
+    # low-rank items are dealt with the calls of most work per item first
+    # (d_in + d_out, ties in call order), item `it` to CTA G - 1 - it % G; each
+    # charges (d_in + d_out) // ITEM_FEATURES_PER_BLOCK stream blocks against
+    # its CTA (host bound of items per call)
+    order = sorted(range(len(calls)), key=lambda i: (-(calls[i]["d_in"] + calls[i]["d_out"]), i))
+    icost = [0] * G
+    it = 0
+    for i in order:
+        k = calls[i]
+        pen = (k["d_in"] + k["d_out"]) // ITEM_FEATURES_PER_BLOCK
+        for _ in range(k["lr_items"]):
+            icost[G - 1 - it % G] += pen
+            it += 1
+    W = blk + t_vs + sum(icost)
     start, vsb, mono = [], 0, True
     for i in range(G + 1):
         start.append(i * W // G - vsb)
         if i < units:
             vsb += ublk[i]
+        if i < G:
+            vsb += icost[i]
         if i > 0 and start[i] < start[i - 1]:
             mono = False
     if not mono or start[0] != 0 or start[G] != blk:
