@@ -355,8 +355,8 @@ def test_prefill_vera_shared_ranks(scute, rv):
 
 def test_tiny_fp32(scute):
     """fp32 single linear, 16 tokens, one adapter per method: max rel <= 1e-4.
-    Also prints the score under the 1e-3 rms(r) floor, the survey's first
-    proposal for the relative floor."""
+    Also prints the score under a 1e-3 rms(r) floor, the tighter choice of
+    relative floor that was weighed against the 1e-2 one used here."""
     w = WL.tiny_fp32()
     ctx = H.make_ctx(scute, w)
     outs = H.run_layers(ctx, w, ["lin"], "fp32")
