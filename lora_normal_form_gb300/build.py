@@ -21,7 +21,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libscute.so")
 
 SOURCES = ["api.cu", "bytemodel.cu", "k_gemm.cu", "k_index.cu", "k_rotate.cu", "k_lowrank.cu", "k_lrtc.cu",
-           "k_fold.cu", "noalloc.cu", "k_step.cu", "k_variant.cu"]
+           "k_fold.cu", "noalloc.cu", "k_step.cu", "k_variant.cu", "k_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -156,6 +156,17 @@ void count_launch(scute_ctx *c, int k) { c->launches += k; }
 // of the hot path is bracketed by an event pair on its stream, tagged with its
 // kind.  Event records made while the stream is being captured become graph
 // nodes, re-recorded on every replay.
+// The device address of a pinned, mapped host buffer (null for pageable
+// memory, device memory, or any pointer the runtime does not know).
+const void *mapped_host(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 struct TimedLaunch {
     scute_ctx *c;
     cudaStream_t st;
@@ -1239,20 +1250,66 @@ scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t osz = out_dtype == SCUTE_FP32 ? 4 : 2;
     scute_call dev[SCUTE_MAX_CALLS];
-    CU_TRY(c, cudaMemcpyAsync(c->st_ids, ids_host, (size_t)n * 4, cudaMemcpyHostToDevice, st));
     for (int i = 0; i < n_calls; ++i) {
-        const LayerRec &L = c->layers[calls[i].layer];
         dev[i].layer = calls[i].layer;
         dev[i].x = reinterpret_cast<uint8_t *>(c->step_hx) + (size_t)i * STEP_MAX_TOKENS * c->step_hx_cols * c->esz;
         dev[i].out = reinterpret_cast<uint8_t *>(c->step_hout) + (size_t)i * STEP_MAX_TOKENS * c->step_hout_cols * 4;
-        CU_TRY(c, cudaMemcpyAsync(const_cast<void *>(dev[i].x), calls[i].x, (size_t)n * L.d_in * c->esz,
-                                  cudaMemcpyHostToDevice, st));
+    }
+    // Pinned, mapped host buffers are moved by one gather launch before the
+    // step and one scatter launch after it (the device reads and writes them
+    // through their device addresses); any other host buffer, by one copy
+    // each.
+    static_assert(COPY_MAX_SEGS >= 2 * SCUTE_MAX_CALLS + 1, "copy segments");
+    CopySegs in{}, outs{};
+    bool gather = true, scatter = true;
+    {
+        const void *d_ids = mapped_host(ids_host);
+        gather = d_ids != nullptr;
+        if (gather) {
+            in.src[in.n] = d_ids;
+            in.dst[in.n] = c->st_ids;
+            in.bytes[in.n++] = (size_t)n * 4;
+        }
+        for (int i = 0; i < n_calls; ++i) {
+            const LayerRec &L = c->layers[calls[i].layer];
+            const void *dx = gather ? mapped_host(calls[i].x) : nullptr;
+            if (!dx) gather = false;
+            if (gather) {
+                in.src[in.n] = dx;
+                in.dst[in.n] = const_cast<void *>(dev[i].x);
+                in.bytes[in.n++] = (size_t)n * L.d_in * c->esz;
+            }
+            void *dout = scatter ? const_cast<void *>(mapped_host(calls[i].out)) : nullptr;
+            if (!dout) scatter = false;
+            if (scatter) {
+                outs.src[outs.n] = dev[i].out;
+                outs.dst[outs.n] = dout;
+                outs.bytes[outs.n++] = (size_t)n * L.d_out * osz;
+            }
+        }
+    }
+    if (gather) {
+        CU_TRY(c, launch_copy_segments(in, st));
+        count_launch(c, 1);
+    } else {
+        CU_TRY(c, cudaMemcpyAsync(c->st_ids, ids_host, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+        for (int i = 0; i < n_calls; ++i) {
+            const LayerRec &L = c->layers[calls[i].layer];
+            CU_TRY(c, cudaMemcpyAsync(const_cast<void *>(dev[i].x), calls[i].x, (size_t)n * L.d_in * c->esz,
+                                      cudaMemcpyHostToDevice, st));
+        }
     }
     s = step_launch(c, dev, n_calls, c->st_ids, (int)n, out_dtype == SCUTE_FP32 ? 1 : 0, st);
     if (s) return s;
-    for (int i = 0; i < n_calls; ++i) {
-        const LayerRec &L = c->layers[calls[i].layer];
-        CU_TRY(c, cudaMemcpyAsync(calls[i].out, dev[i].out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost, st));
+    if (scatter) {
+        CU_TRY(c, launch_copy_segments(outs, st));
+        count_launch(c, 1);
+    } else {
+        for (int i = 0; i < n_calls; ++i) {
+            const LayerRec &L = c->layers[calls[i].layer];
+            CU_TRY(c, cudaMemcpyAsync(calls[i].out, dev[i].out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost,
+                                      st));
+        }
     }
     return SCUTE_OK;
 }

@@ -282,6 +282,18 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
                          int *perm, int *aid_s, int *seg_start, int *seg_aid, IndexMeta *meta,
                          int *status, cudaStream_t st, int *seg_unit = nullptr, int *seg_tile = nullptr);
 
+// Copies of up to COPY_MAX_SEGS buffers in one launch (k_copy.cu): each
+// source and destination a device-visible address (device memory, or the
+// device address of pinned, mapped host memory).
+constexpr int COPY_MAX_SEGS = 2 * 8 + 1;
+struct CopySegs {
+    const void *src[COPY_MAX_SEGS];
+    void *dst[COPY_MAX_SEGS];
+    size_t bytes[COPY_MAX_SEGS];
+    int n;
+};
+cudaError_t launch_copy_segments(const CopySegs &s, cudaStream_t st);
+
 cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const int *perm,
                                  const int *aid_s, const Slot *slots, void *xs, int kdim,
                                  cudaStream_t st, bool pdl);

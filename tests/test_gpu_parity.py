@@ -476,6 +476,43 @@ def test_linear_host_matches_linear(scute):
     ctx.close()
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_linear_batch_host_matches_linear_batch(scute, pinned, out_dtype):
+    """scute_linear_batch_host over several layers: pinned host buffers go
+    through one gather launch before the step and one scatter launch after it,
+    pageable ones through a copy each; both equal the device-buffer call bit
+    for bit."""
+    w = _small_decode(n=40)
+    names = list(SMALL_NAMES)
+    ctx = H.make_ctx(scute, w)
+    dt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    ids_dev = torch.from_numpy(w.ids.copy()).cuda()
+    xs, outs_dev, calls_h = {}, {}, []
+    for name in names:
+        L = w.layer(name)
+        xs[name] = torch.from_numpy(L.get("x").view(np.int16)).view(torch.bfloat16)
+        outs_dev[name] = torch.empty(w.n, L.d_out, dtype=dt, device="cuda")
+    ctx.linear_batch([(xs[nm].cuda(), ctx.layer_ids[nm], outs_dev[nm]) for nm in names], ids_dev, out_dtype)
+    torch.cuda.synchronize()
+    ids_h = torch.from_numpy(w.ids.copy())
+    outs_h = {nm: torch.empty(w.n, w.layer(nm).d_out, dtype=dt) for nm in names}
+    if pinned:
+        ids_h = ids_h.pin_memory()
+        xs = {nm: t.pin_memory() for nm, t in xs.items()}
+        outs_h = {nm: t.pin_memory() for nm, t in outs_h.items()}
+    n0 = ctx.launch_count()
+    ctx.linear_batch_host([(xs[nm], ctx.layer_ids[nm], outs_h[nm]) for nm in names], ids_h, out_dtype,
+                          stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    # the step, plus the gather and the scatter launch for pinned buffers
+    assert ctx.launch_count() - n0 == (3 if pinned else 1)
+    assert ctx.sync_status() == 0
+    for nm in names:
+        assert torch.equal(outs_h[nm], outs_dev[nm].cpu()), nm
+    ctx.close()
+
+
 def test_cuda_graph_replay_matches_eager(scute):
     w = _small_decode(n=40)
     ctx = H.make_ctx(scute, w)
