@@ -1279,13 +1279,6 @@ scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int 
                 in.dst[in.n] = const_cast<void *>(dev[i].x);
                 in.bytes[in.n++] = (size_t)n * L.d_in * c->esz;
             }
-            void *dout = scatter ? const_cast<void *>(mapped_host(calls[i].out)) : nullptr;
-            if (!dout) scatter = false;
-            if (scatter) {
-                outs.src[outs.n] = dev[i].out;
-                outs.dst[outs.n] = dout;
-                outs.bytes[outs.n++] = (size_t)n * L.d_out * osz;
-            }
         }
     }
     if (gather) {
@@ -1301,6 +1294,18 @@ scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int 
     }
     s = step_launch(c, dev, n_calls, c->st_ids, (int)n, out_dtype == SCUTE_FP32 ? 1 : 0, st);
     if (s) return s;
+    // the output buffers are looked up while the step runs
+    for (int i = 0; scatter && i < n_calls; ++i) {
+        const LayerRec &L = c->layers[calls[i].layer];
+        void *dout = const_cast<void *>(mapped_host(calls[i].out));
+        if (!dout) {
+            scatter = false;
+            break;
+        }
+        outs.src[outs.n] = dev[i].out;
+        outs.dst[outs.n] = dout;
+        outs.bytes[outs.n++] = (size_t)n * L.d_out * osz;
+    }
     if (scatter) {
         CU_TRY(c, launch_copy_segments(outs, st));
         count_launch(c, 1);
