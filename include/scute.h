@@ -221,8 +221,11 @@ scute_status scute_linear_batch(scute_ctx *ctx, const scute_call *calls, int n_c
 
 /* scute_linear_batch with HOST buffers (every x and out, and adapter_ids, in
  * host memory): the inputs are copied into context-owned device staging, the
- * batch runs, the outputs are copied back, all enqueued on `stream`.  The
- * caller synchronises the stream before reading the outputs. */
+ * batch runs, the outputs are copied back, all enqueued on `stream`.  When
+ * every input (or every output) buffer is pinned and mapped, one kernel
+ * launch moves all of them through their device addresses; otherwise each
+ * buffer is one asynchronous copy.  The caller synchronises the stream before
+ * reading the outputs. */
 scute_status scute_linear_batch_host(scute_ctx *ctx, const scute_call *calls, int n_calls,
                                      const int32_t *ids_host, int64_t n, scute_dtype out_dtype,
                                      void *stream);
