@@ -310,7 +310,9 @@ scute_status scute_index_tokens_noalloc(const int8_t *method_of_adapter, int32_t
  * (scute_set_variant; the step's own bytes then lose R, or the DoRA and
  * (IA)^3 s vectors); otherwise each layer takes the per-kernel plan
  * ("index", "rotate", "base_gemm", "lr_shrink", "lr_expand", "vera_shrink",
- * "vera_expand").  Pure host arithmetic: no device work, no context needed for
+ * "vera_expand"; in a bf16 context above 256 tokens "lr_shrink" and, for a
+ * shared rank that is a multiple of 64, "vera_shrink" come before
+ * "base_gemm", which takes in the owned expand).  Pure host arithmetic: no device work, no context needed for
  * scute_byte_model and scute_byte_model_batch. */
 #define SCUTE_BM_MAX_KERNELS 64
 typedef struct {

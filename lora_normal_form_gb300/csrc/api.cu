@@ -996,6 +996,10 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         int kchunk = 0;
         lr_ks = lowrank_ks(L.d_in, &kchunk);
     }
+    // VeRA shared shrink on the tensor cores (bf16, many VeRA rows); right
+    // after the tensor-core owned shrink it runs beside that launch
+    const bool vs_tc = vera_on && !f32 && tok_on_p && L.rv % 64 == 0 && c->vs_part_cols >= (size_t)L.rv;
+    const bool vs_after_lr = vs_tc && lr_fused && L.n_rot_lr == 0;
     // owned low-rank shrink (and, unless fused, its expand).  bf16: the shrink
     // runs on the tensor cores over the sorted token operand, which holds x
     // itself for every owned-term row unless an adapter of the layer has both
@@ -1021,7 +1025,8 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
             q.status = c->d_status;
             const int tile_bound = (nn + SEG_TILE_ROWS - 1) / SEG_TILE_ROWS + (reg + 1 < nn ? reg + 1 : nn);
             const int units = tile_bound * q.ks;
-            CU_TRY(c, launch_lr_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
+            CU_TRY(c, launch_lr_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl,
+                                          vs_after_lr && !expand));
         }
         if (!tc || expand)
             CU_TRY(c, launch_lowrank(f32, x, L.d_in, L.d_out, unit_bound, c->d_perm, c->d_seg_start, c->d_seg_aid,
@@ -1035,6 +1040,38 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
     if (lr_fused) {
         const scute_status e = owned_lowrank(false);
         if (e != SCUTE_OK) return e;
+    }
+    // 3b. VeRA shared shrink over the VeRA rows, bf16 with many VeRA rows:
+    // K-split units on the tensor cores, so that every SM streams (one CTA per
+    // 128 x rank tile over all of K would leave most of them idle).  It needs
+    // neither the owned shrink nor the base GEMM, so it comes before the GEMM
+    if (vs_tc) {
+        VsTcArgs q;
+        memset(&q, 0, sizeof(q));
+        q.mapX = L.mapXs;
+        q.mapA = L.mapAsh;
+        q.kblocks = (L.d_in + 63) / 64;
+        // at most VS_KS chunks, none of them empty
+        q.chunk_blocks = (q.kblocks + VS_KS - 1) / VS_KS;
+        q.ks = (q.kblocks + q.chunk_blocks - 1) / q.chunk_blocks;
+        q.n_nt = L.rv / 64;
+        q.rv = L.rv;
+        q.ldu = L.krv;
+        q.max_tokens = c->max_tokens;
+        q.meta = c->d_meta;
+        q.aid_s = c->d_aid;
+        q.slots = slots;
+        q.part = c->vs_part;
+        q.ctr = c->vs_ctr;
+        q.U = c->U;
+        q.status = c->d_status;
+        q.after_lr = vs_after_lr ? 1 : 0;
+        const int units = (nn + 127) / 128 * q.n_nt * q.ks;
+        if (VS_CTR_TILES + (nn + 127) / 128 * q.n_nt > VS_CTR_INTS)
+            return fail(c, SCUTE_ERR_UNSUPPORTED, "VeRA shrink counters too few for this batch");
+        CU_TRY(c, tl.begin());
+        CU_TRY(c, launch_vera_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
+        CU_TRY(c, tl.end(SCUTE_KIND_VERA_SHRINK));
     }
     // 4. base GEMM with the s / b (and fused owned low-rank) epilogue
     GemmArgs g;
@@ -1114,38 +1151,11 @@ scute_status scute_linear(scute_ctx *c, const void *x, const int32_t *ids, int64
         v.part = c->gpart;
         v.part_stride = (long long)pv.bn * 128;
         v.n_ft = tok_on_p ? (L.rv + pv.bn - 1) / pv.bn : (L.rv + 127) / 128;
-        CU_TRY(c, tl.begin());
-        if (!f32 && tok_on_p && L.rv % 64 == 0 && c->vs_part_cols >= (size_t)L.rv) {
-            // many VeRA rows: K-split units on the tensor cores, so that every
-            // SM streams (one CTA per 128 x rank tile over all of K leaves most
-            // of them idle)
-            VsTcArgs q;
-            memset(&q, 0, sizeof(q));
-            q.mapX = L.mapXs;
-            q.mapA = L.mapAsh;
-            q.kblocks = (L.d_in + 63) / 64;
-            // at most VS_KS chunks, none of them empty
-            q.chunk_blocks = (q.kblocks + VS_KS - 1) / VS_KS;
-            q.ks = (q.kblocks + q.chunk_blocks - 1) / q.chunk_blocks;
-            q.n_nt = L.rv / 64;
-            q.rv = L.rv;
-            q.ldu = L.krv;
-            q.max_tokens = c->max_tokens;
-            q.meta = c->d_meta;
-            q.aid_s = c->d_aid;
-            q.slots = slots;
-            q.part = c->vs_part;
-            q.ctr = c->vs_ctr;
-            q.U = c->U;
-            q.status = c->d_status;
-            const int units = (nn + 127) / 128 * q.n_nt * q.ks;
-            if (VS_CTR_TILES + (nn + 127) / 128 * q.n_nt > VS_CTR_INTS)
-                return fail(c, SCUTE_ERR_UNSUPPORTED, "VeRA shrink counters too few for this batch");
-            CU_TRY(c, launch_vera_shrink_tc(q, units < c->num_sms ? units : c->num_sms, st, c->pdl));
-        } else {
+        if (!vs_tc) {
+            CU_TRY(c, tl.begin());
             CU_TRY(c, launch_gemm(v, pv, st, c->pdl));
+            CU_TRY(c, tl.end(SCUTE_KIND_VERA_SHRINK));
         }
-        CU_TRY(c, tl.end(SCUTE_KIND_VERA_SHRINK));
 
         GemmArgs e = v;
         e.mapP = tok_on_p ? L.mapU : L.mapBsh;

@@ -101,7 +101,9 @@ bool count_layer(const scute_bm_layer *L, const int32_t *ids, int64_t n, LayerCo
 // owned low-rank shrink and expand, VeRA shrink and expand GEMMs.  In bf16
 // contexts with more than 256 tokens the owned shrink runs before the base
 // GEMM and the owned expand inside its epilogue (the GEMM then also reads the
-// partial v and each B', and writes out once).
+// partial v and each B', and writes out once); there the VeRA shrink of a
+// shared rank that is a multiple of 64 (its tensor-core form) also comes
+// before the base GEMM.
 void per_kernel_plan(const scute_bm_layer *L, const LayerCount &c, scute_byte_report *rep) {
     const int64_t n = c.n, E = c.E, Eo = c.Eo;
     const int64_t index_out = 8 * n + 4 * (c.segs + 1) + 4 * c.segs + 88;
@@ -110,7 +112,13 @@ void per_kernel_plan(const scute_bm_layer *L, const LayerCount &c, scute_byte_re
     add_kernel(rep, "index", 4 * n + index_out, 0);
     add_kernel(rep, "rotate", n * c.din * E + 8 * n + c.R + n * c.kd * E, 2 * c.n_rot * c.din * 32);
     const int64_t shrink_b = c.n_lr * c.din * E + c.A + ks * c.lr_rank_rows * 4;
+    const int64_t shA = c.n_v > 0 ? c.rv * c.kd * E : 0;
+    const int64_t shB = c.n_v > 0 ? c.dout * c.krv * E : 0;
+    const int64_t vshrink_b = c.n_v * c.kd * E + shA + c.d + c.n_v * c.krv * E;
+    const int64_t vshrink_f = 2 * c.n_v * c.rv * c.kd;
+    const bool vs_first = L->vera_launched && L->dtype != SCUTE_FP32 && n > 256 && c.rv % 64 == 0;
     if (fused) add_kernel(rep, "lr_shrink", shrink_b, 2 * c.lr_rank_rows * c.din);
+    if (vs_first) add_kernel(rep, "vera_shrink", vshrink_b, vshrink_f);
     int64_t gemm_b = c.dout * c.kd * E + n * c.kd * E + c.sb + 8 * n + n * c.dout * Eo;
     int64_t gemm_f = 2 * n * c.kd * c.dout;
     if (fused) {
@@ -124,9 +132,7 @@ void per_kernel_plan(const scute_bm_layer *L, const LayerCount &c, scute_byte_re
                    2 * c.lr_rank_rows * c.dout);
     }
     if (L->vera_launched) {
-        const int64_t shA = c.n_v > 0 ? c.rv * c.kd * E : 0;
-        const int64_t shB = c.n_v > 0 ? c.dout * c.krv * E : 0;
-        add_kernel(rep, "vera_shrink", c.n_v * c.kd * E + shA + c.d + c.n_v * c.krv * E, 2 * c.n_v * c.rv * c.kd);
+        if (!vs_first) add_kernel(rep, "vera_shrink", vshrink_b, vshrink_f);
         add_kernel(rep, "vera_expand", c.n_v * c.krv * E + shB + c.e + 2 * c.n_v * c.dout * Eo,
                    2 * c.n_v * c.krv * c.dout);
     }

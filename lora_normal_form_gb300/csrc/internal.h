@@ -325,7 +325,7 @@ struct LrTcArgs {
     float *v_part;             // [ks][max_tokens][MAX_RANK]
     int *status;
 };
-size_t lr_shrink_tc_smem_bytes();
+size_t shrink_tc_smem_bytes(int stages);
 // VeRA shared shrink on the tensor cores for prefill-sized batches (bf16,
 // shared rank a multiple of 64): units of 128 VeRA rows x 64 shared ranks x
 // one of ks K chunks; partial tiles in `part`, the last unit of a tile sums
@@ -347,9 +347,11 @@ struct VsTcArgs {
     int *ctr;
     void *U;                   // bf16 [VeRA rows][ldu]
     int *status;
+    int after_lr;              // launched right after the tensor-core low-rank shrink
 };
 cudaError_t launch_vera_shrink_tc(const VsTcArgs &p, int grid, cudaStream_t st, bool pdl);
-cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl);
+// beside: a VeRA shrink is launched right after it, to run beside it
+cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl, bool beside);
 
 // registration-time kernels
 cudaError_t launch_transpose_w(bool f32, const void *W, int rows, int cols, void *Wt, int kdim,

@@ -32,7 +32,14 @@ namespace scute {
 namespace {
 
 constexpr int THREADS = 192;
-constexpr int STAGES = 6;
+// Pipeline stages: 6 for a shrink that has the SMs to itself; fewer when the
+// low-rank and the VeRA shrink run side by side, so that a CTA of each fits in
+// one SM's shared memory (BESIDE_LR + BESIDE_VS stages of 24 KB, plus two
+// control blocks and alignment pads, within 227 KB)
+constexpr int STAGES_ALONE = 6;
+constexpr int BESIDE_LR = 4;
+constexpr int BESIDE_VS = 5;
+constexpr int MAX_STAGES = 6;
 constexpr int TILE_ROWS = 128;
 constexpr int BOX_ROWS = 64;
 constexpr int BOX_BYTES = BOX_ROWS * 128;
@@ -43,8 +50,8 @@ constexpr int ACC_COLS = 64;          // one accumulator: up to 64 ranks
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 struct Ctrl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -53,6 +60,9 @@ struct Ctrl {
 };
 constexpr int CTRL_BYTES = 256;
 static_assert(sizeof(Ctrl) <= CTRL_BYTES, "control block");
+static_assert(BESIDE_LR <= MAX_STAGES && BESIDE_VS <= MAX_STAGES && STAGES_ALONE <= MAX_STAGES, "stages");
+static_assert(2 * (1024 + CTRL_BYTES) + (BESIDE_LR + BESIDE_VS) * (XB + AB) + 2 * 1024 <= 228 * 1024,
+              "a low-rank and a VeRA shrink CTA side by side in one SM");
 
 // K-major tile in the 128-byte-swizzle layout TMA writes (8-row atoms of
 // 1024 bytes stacked along M / N).
@@ -125,20 +135,25 @@ __device__ __forceinline__ bool unit_at(const LrTcArgs &p, int u, Unit &U) {
     return true;
 }
 
+template <int NST>
 __global__ void __launch_bounds__(THREADS, 1) lr_shrink_tc_kernel(const __grid_constant__ LrTcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + NST * STAGE);
     volatile int *abort_flag = &ctrl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // the segments come from the indexing kernel, the token rows from the
-    // rotation kernel: wait for the previous launches before reading either
+    // rotation kernel: wait for the previous launches before reading either.
+    // The next launch may start at once: a VeRA shrink reads nothing written
+    // here and waits for this grid only before it exits; the base GEMM waits
+    // for it before it reads v
     ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctrl->full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&ctrl->empty[s]), 1);
         }
@@ -180,15 +195,15 @@ __global__ void __launch_bounds__(THREADS, 1) lr_shrink_tc_kernel(const __grid_c
                     ptx::tma_load_2d(sX + BOX_BYTES, &p.mapX, kb * 64, U.r0 + BOX_ROWS, fb);
                     ptx::tma_load_2d(sX + XB, U.mapA, kb * 64, 0, fb);
                     ++issued;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
             }
         prod_done:
             // every issued copy must have landed before the CTA may exit
             {
-                const int m_max = issued < STAGES ? (int)issued : STAGES;
+                const int m_max = issued < NST ? (int)issued : NST;
                 for (int m = 1; m <= m_max; ++m) {
-                    const int s = (stage - m + STAGES) % STAGES;
+                    const int s = (stage - m + NST) % NST;
                     const uint32_t ph = (s < stage) ? phase : (phase ^ 1);
                     wait_bar(ptx::smem_u32(&ctrl->full[s]), ph, abort_flag, false);
                 }
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, 1) lr_shrink_tc_kernel(const __grid_c
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(ptx::smem_u32(&ctrl->empty[stage]));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
                 ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
@@ -270,8 +285,6 @@ __global__ void __launch_bounds__(THREADS, 1) lr_shrink_tc_kernel(const __grid_c
         ptx::tmem_dealloc(tmem, 2 * ACC_COLS);
     }
     if (threadIdx.x == 0 && ctrl->abort) atomicOr(p.status, STATUS_TIMEOUT);
-    // the expand kernel may start its set-up once every CTA is past here
-    ptx::grid_dep_launch();
 }
 
 // ---------------------------------------------------------------- VeRA shared shrink
@@ -296,23 +309,28 @@ __device__ __forceinline__ bool vs_all(bool v) {
     return r != 0;
 }
 
+template <int NST>
 __global__ void __launch_bounds__(THREADS, 1) vera_shrink_tc_kernel(const __grid_constant__ VsTcArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + STAGES * STAGE);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + NST * STAGE);
     __shared__ int s_last;
     volatile int *abort_flag = &ctrl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    ptx::grid_dep_wait();   // segments and token rows come from earlier launches
+    // segments and token rows come from earlier launches.  Launched right
+    // after the low-rank shrink (which starts its dependents once its own wait
+    // is over, so both are complete here), it runs beside that grid and waits
+    // for it only before it exits, so that the launch after this one sees v
+    if (!p.after_lr) ptx::grid_dep_wait();
     const int base = p.meta->offset[RANK_VERA], count = p.meta->count[RANK_VERA];
     const int n_rt = (count + TILE_ROWS - 1) / TILE_ROWS;
     const int per_rt = p.n_nt * p.ks;
     const int n_units = n_rt * per_rt;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(ptx::smem_u32(&ctrl->full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&ctrl->empty[s]), 1);
         }
@@ -353,14 +371,14 @@ __global__ void __launch_bounds__(THREADS, 1) vera_shrink_tc_kernel(const __grid
                     ptx::tma_load_2d(sX + BOX_BYTES, &p.mapX, kb * 64, base + rt * TILE_ROWS + BOX_ROWS, fb);
                     ptx::tma_load_2d(sX + XB, &p.mapA, kb * 64, nt * 64, fb);
                     ++issued;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
             }
         prod_done:
             {
-                const int m_max = issued < STAGES ? (int)issued : STAGES;
+                const int m_max = issued < NST ? (int)issued : NST;
                 for (int m = 1; m <= m_max; ++m) {
-                    const int s = (stage - m + STAGES) % STAGES;
+                    const int s = (stage - m + NST) % NST;
                     const uint32_t ph = (s < stage) ? phase : (phase ^ 1);
                     wait_bar(ptx::smem_u32(&ctrl->full[s]), ph, abort_flag, false);
                 }
@@ -390,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1) vera_shrink_tc_kernel(const __grid
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_bf16(d_tmem, da + 2 * kk, db + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(ptx::smem_u32(&ctrl->empty[stage]));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == NST) { stage = 0; phase ^= 1; }
                 }
                 ptx::mma_commit(ptx::smem_u32(&ctrl->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
@@ -495,49 +513,48 @@ __global__ void __launch_bounds__(THREADS, 1) vera_shrink_tc_kernel(const __grid
             __threadfence();
         }
     }
+    if (p.after_lr) ptx::grid_dep_wait();
     ptx::grid_dep_launch();
 }
 
 }  // namespace
 
-size_t lr_shrink_tc_smem_bytes() { return 1024 + (size_t)STAGES * STAGE + CTRL_BYTES; }
+size_t shrink_tc_smem_bytes(int stages) { return 1024 + (size_t)stages * STAGE + CTRL_BYTES; }
 
-cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl) {
-    static std::atomic<unsigned long long> attr_done{0};
+namespace {
+
+template <typename Args>
+cudaError_t launch_shrink(void (*kernel)(Args), std::atomic<unsigned long long> &done, const Args &p, int grid,
+                          int stages, cudaStream_t st, bool pdl) {
     {
-        const cudaError_t e = allow_max_dynamic_smem(lr_shrink_tc_kernel, attr_done);
+        const cudaError_t e = allow_max_dynamic_smem(kernel, done);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = lr_shrink_tc_smem_bytes();
+    cfg.dynamicSmemBytes = shrink_tc_smem_bytes(stages);
     cfg.stream = st;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, lr_shrink_tc_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace
+
+cudaError_t launch_lr_shrink_tc(const LrTcArgs &p, int grid, cudaStream_t st, bool pdl, bool beside) {
+    static std::atomic<unsigned long long> done_alone{0}, done_beside{0};
+    if (beside) return launch_shrink(lr_shrink_tc_kernel<BESIDE_LR>, done_beside, p, grid, BESIDE_LR, st, pdl);
+    return launch_shrink(lr_shrink_tc_kernel<STAGES_ALONE>, done_alone, p, grid, STAGES_ALONE, st, pdl);
 }
 
 cudaError_t launch_vera_shrink_tc(const VsTcArgs &p, int grid, cudaStream_t st, bool pdl) {
-    static std::atomic<unsigned long long> attr_done{0};
-    {
-        const cudaError_t e = allow_max_dynamic_smem(vera_shrink_tc_kernel, attr_done);
-        if (e != cudaSuccess) return e;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = lr_shrink_tc_smem_bytes();
-    cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, vera_shrink_tc_kernel, p);
+    static std::atomic<unsigned long long> done_alone{0}, done_beside{0};
+    if (p.after_lr) return launch_shrink(vera_shrink_tc_kernel<BESIDE_VS>, done_beside, p, grid, BESIDE_VS, st, pdl);
+    return launch_shrink(vera_shrink_tc_kernel<STAGES_ALONE>, done_alone, p, grid, STAGES_ALONE, st, pdl);
 }
 
 }  // namespace scute

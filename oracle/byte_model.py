@@ -99,7 +99,8 @@ def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool, lr_fused: b
     With ``lr_fused`` (bf16 contexts, more than 256 tokens) the owned shrink
     runs before the base GEMM and the owned expand inside the GEMM's epilogue:
     the GEMM then also reads the shrink's partial v and each B', and out is
-    written once."""
+    written once.  There the VeRA shrink of a shared rank that is a multiple
+    of 64 (its tensor-core form) also comes before the base GEMM."""
     n, E, Eo, kd, d_in, d_out = c["n"], c["E"], c["Eo"], c["kd"], c["d_in"], c["d_out"]
     rv, krv = c["rv"], c["krv"]
     index_out = 8 * n + 4 * (c["segments"] + 1) + 4 * c["segments"] + 88
@@ -119,18 +120,23 @@ def _per_kernel_plan(c, lowrank_launched: bool, vera_launched: bool, lr_fused: b
         # x in, perm/ids in, R of each distinct rotating adapter, x' out
         ("rotate", n * d_in * E + 8 * n + c["R_b"] + n * kd * E, 2 * c["n_rot"] * d_in * 32),
     ]
+    n_v = c["n_v"]
+    shA = rv * kd * E if n_v else 0
+    shB = d_out * krv * E if n_v else 0
+    vshrink = ("vera_shrink", n_v * kd * E + shA + c["d_b"] + n_v * krv * E, 2 * n_v * rv * kd)
+    vs_first = vera_launched and lr_fused and rv % 64 == 0
     if fused:
         kernels.append(shrink)
+    if vs_first:
+        kernels.append(vshrink)
     kernels.append(("base_gemm", gemm_b, gemm_f))
     if lowrank_launched and not fused:
         kernels.append(shrink)
         kernels.append(("lr_expand", ks * c["lr_rank_rows"] * 4 + c["B_b"] + 2 * c["n_lr"] * d_out * Eo,
                         2 * c["lr_rank_rows"] * d_out))
     if vera_launched:
-        n_v = c["n_v"]
-        shA = rv * kd * E if n_v else 0
-        shB = d_out * krv * E if n_v else 0
-        kernels.append(("vera_shrink", n_v * kd * E + shA + c["d_b"] + n_v * krv * E, 2 * n_v * rv * kd))
+        if not vs_first:
+            kernels.append(vshrink)
         kernels.append(("vera_expand", n_v * krv * E + shB + c["e_b"] + 2 * n_v * d_out * Eo,
                         2 * n_v * krv * d_out))
     return kernels

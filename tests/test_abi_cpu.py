@@ -202,9 +202,11 @@ def test_batch_byte_model_matches_oracle(lib):
 def test_fused_expand_plan_moves_only_the_out_rewrite():
     """bf16 batches above 256 tokens run the owned expand inside the base
     GEMM's epilogue.  Against the separate expand the launch list loses
-    lr_expand, the shrink comes before the GEMM, the GEMM gains the expand's
-    v partials, B' and flops, and the total bytes drop by exactly the owned
-    rows of out read and written once more; the flops are unchanged."""
+    lr_expand, the shrink comes before the GEMM (and the tensor-core VeRA
+    shrink, for a shared rank that is a multiple of 64, right after it), the
+    GEMM gains the expand's v partials, B' and flops, and the total bytes drop
+    by exactly the owned rows of out read and written once more; the flops are
+    unchanged."""
     w = WL.prefill_mixed(n_req=6, lo=40, hi=200, shapes=WL.SMALL_PROJ, proj=("q", "k", "up", "down"))
     assert w.n > 256
     for layer in ("q", "up"):
@@ -214,9 +216,14 @@ def test_fused_expand_plan_moves_only_the_out_rewrite():
         sep = OBM._per_kernel_plan(c, lowrank, vera, lr_fused=False)
         fus = OBM._per_kernel_plan(c, lowrank, vera, lr_fused=True)
         names_sep, names_fus = [k[0] for k in sep], [k[0] for k in fus]
+        vs_first = vera and L.shared_rank % 64 == 0
         assert names_sep[:5] == ["index", "rotate", "base_gemm", "lr_shrink", "lr_expand"]
-        assert names_fus[:4] == ["index", "rotate", "lr_shrink", "base_gemm"]
-        assert "lr_expand" not in names_fus and names_fus[4:] == names_sep[5:]
+        head = ["index", "rotate", "lr_shrink"] + (["vera_shrink"] if vs_first else []) + ["base_gemm"]
+        assert names_fus[:len(head)] == head
+        rest_sep = [k for k in names_sep[5:] if not (vs_first and k == "vera_shrink")]
+        assert "lr_expand" not in names_fus and names_fus[len(head):] == rest_sep
+        if vera:
+            assert dict((k[0], k) for k in sep)["vera_shrink"] == dict((k[0], k) for k in fus)["vera_shrink"]
         ks = OBM.lowrank_ks(L.d_in)
         g_sep, g_fus = dict((k[0], k) for k in sep)["base_gemm"], dict((k[0], k) for k in fus)["base_gemm"]
         assert g_fus[1] - g_sep[1] == ks * c["lr_rank_rows"] * 4 + c["B_b"]
