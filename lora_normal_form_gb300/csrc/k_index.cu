@@ -16,10 +16,12 @@
 // STATUS_BAD_ADAPTER.
 //
 // Sort: each token becomes the 32-bit word (key << 16) | token, sorted by a
-// two-pass least-significant-digit counting sort on the key's two bytes.  A pass
-// is stable: warp w owns a contiguous run of the input, counts digits with
-// __match_any_sync, and scatters in order through per-(warp, digit) offsets laid
-// out digit-major, warp-minor.
+// least-significant-digit counting sort on the key.  The keys are below
+// 6 A + 1 (A = the adapter ids' bound), so for A <= 85 one pass on a digit of
+// 8 or 9 bits orders them completely; otherwise two passes take the key's two
+// bytes.  A pass is stable: warp w owns a contiguous run of the input, counts
+// digits with __match_any_sync, and scatters in order through per-(warp,
+// digit) offsets laid out digit-major, warp-minor.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -57,6 +59,9 @@ __device__ int block_excl_scan(int v, int *s_warp, int *total) {
     return r;
 }
 
+// One stable pass on the digit (v >> shift) & (DIG - 1); DIG <= blockDim.x
+// (256 or 512 digits; hist holds nw x DIG counters).
+template <int DIG>
 __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift, int *hist,
                            int *s_warp) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
@@ -64,29 +69,30 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
     chunk = (chunk + 31) & ~31;
     const int beg = w * chunk;
     const int end = min(n, beg + chunk);
-    for (int i = tid; i < nw * 256; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < nw * DIG; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int base = beg; base < end; base += 32) {
         const int i = base + lane;
         const bool valid = i < end;
-        const uint32_t d = valid ? ((src[i] >> shift) & 255u) : (256u + lane);
+        // lanes past the end get distinct digits no valid lane has
+        const uint32_t d = valid ? ((src[i] >> shift) & (uint32_t)(DIG - 1)) : ((uint32_t)DIG + lane);
         const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (valid && lane == __ffs(peers) - 1) hist[w * 256 + d] += __popc(peers);
+        if (valid && lane == __ffs(peers) - 1) hist[w * DIG + d] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
     int tot = 0;
-    if (tid < 256) {
+    if (tid < DIG) {
 #pragma unroll 8
-        for (int k = 0; k < nw; ++k) tot += hist[k * 256 + tid];
+        for (int k = 0; k < nw; ++k) tot += hist[k * DIG + tid];
     }
-    const int excl = block_excl_scan(tid < 256 ? tot : 0, s_warp, nullptr);
-    if (tid < 256) {
+    const int excl = block_excl_scan(tid < DIG ? tot : 0, s_warp, nullptr);
+    if (tid < DIG) {
         int run = excl;
 #pragma unroll 8
         for (int k = 0; k < nw; ++k) {
-            const int c = hist[k * 256 + tid];
-            hist[k * 256 + tid] = run;
+            const int c = hist[k * DIG + tid];
+            hist[k * DIG + tid] = run;
             run += c;
         }
     }
@@ -96,14 +102,14 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
         const int i = base + lane;
         const bool valid = i < end;
         const uint32_t v = valid ? src[i] : 0u;
-        const uint32_t d = valid ? ((v >> shift) & 255u) : (256u + lane);
+        const uint32_t d = valid ? ((v >> shift) & (uint32_t)(DIG - 1)) : ((uint32_t)DIG + lane);
         const uint32_t peers = __match_any_sync(0xffffffffu, d);
         int pos = 0;
-        if (valid) pos = hist[w * 256 + d] + __popc(peers & lt);
+        if (valid) pos = hist[w * DIG + d] + __popc(peers & lt);
         __syncwarp();
         if (valid) {
             dst[pos] = v;
-            if (lane == __ffs(peers) - 1) hist[w * 256 + d] += __popc(peers);
+            if (lane == __ffs(peers) - 1) hist[w * DIG + d] += __popc(peers);
         }
         __syncwarp();
     }
@@ -113,7 +119,7 @@ __device__ void radix_pass(const uint32_t *src, uint32_t *dst, int n, int shift,
 __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, const int8_t *method_tab,
                                                      int A, int *perm, int *aid_s, int *seg_start,
                                                      int *seg_aid, IndexMeta *meta, int *status,
-                                                     int *seg_unit, int *seg_tile) {
+                                                     int *seg_unit, int *seg_tile, int key_bits) {
     extern __shared__ uint32_t sm[];
     uint32_t *bufA = sm;
     uint32_t *bufB = sm + n;
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     const uint32_t base_key = (uint32_t)RANK_BASE * (uint32_t)A;
     // every id of this thread is requested, then every method-table entry:
     // two rounds of loads instead of two per id
-    // ids per thread, at most: n <= 2048 runs 256 threads, larger n 1024
+    // ids per thread, at most: n <= 2048 runs 256 or 512 threads, larger n 1024
     constexpr int PER_T = INDEX_MAX_TOKENS / 1024;
     static_assert(PER_T * 256 >= 2048, "ids per thread for the 256-thread launch");
     int idv[PER_T], mv[PER_T];
@@ -154,13 +160,26 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
         bufA[t] = (key << 16) | (uint32_t)t;
     }
     __syncthreads();
-    radix_pass(bufA, bufB, n, 16, hist, s_warp);
-    radix_pass(bufB, bufA, n, 24, hist, s_warp);
+    // keys of at most key_bits bits: one pass (the sorted words land in bufB)
+    // or two (back in bufA); `spare` is the other buffer
+    uint32_t *sorted = bufA, *spare = bufB;
+    if (key_bits <= 8) {
+        radix_pass<256>(bufA, bufB, n, 16, hist, s_warp);
+        sorted = bufB;
+        spare = bufA;
+    } else if (key_bits == 9) {
+        radix_pass<512>(bufA, bufB, n, 16, hist, s_warp);
+        sorted = bufB;
+        spare = bufA;
+    } else {
+        radix_pass<256>(bufA, bufB, n, 16, hist, s_warp);
+        radix_pass<256>(bufB, bufA, n, 24, hist, s_warp);
+    }
 
     // the per-row outputs, with consecutive threads on consecutive rows (one
     // SM writes them all: a strided pattern would cost a store sector per row)
     for (int i = tid; i < n; i += blockDim.x) {
-        const uint32_t v = bufA[i];
+        const uint32_t v = sorted[i];
         const uint32_t key = v >> 16;
         const int rank = (int)(key / (uint32_t)A);
         perm[i] = (int)(v & 0xFFFFu);
@@ -171,16 +190,16 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     const int r0 = min(n, tid * per), r1 = min(n, r0 + per);
     int nflag = 0;
     for (int i = r0; i < r1; ++i)
-        if (i == 0 || (bufA[i - 1] >> 16) != (bufA[i] >> 16)) ++nflag;
+        if (i == 0 || (sorted[i - 1] >> 16) != (sorted[i] >> 16)) ++nflag;
     int total = 0;
     int s = block_excl_scan(nflag, s_warp, &total);
     for (int i = r0; i < r1; ++i) {
-        const uint32_t key = bufA[i] >> 16;
-        if (i == 0 || (bufA[i - 1] >> 16) != key) {
+        const uint32_t key = sorted[i] >> 16;
+        if (i == 0 || (sorted[i - 1] >> 16) != key) {
             const int rank = (int)(key / (uint32_t)A);
             seg_start[s] = i;
             seg_aid[s] = rank >= RANK_BASE ? -1 : (int)(key - (uint32_t)rank * (uint32_t)A);
-            bufB[s] = (uint32_t)rank;   // (bufB is free after the second pass)
+            spare[s] = (uint32_t)rank;   // (free once the sort is done)
             ++s;
         }
     }
@@ -189,7 +208,7 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     // rows and segments per method, one shared atomic per segment (one per
     // row would serialise on the few method counters)
     for (int q = tid; q < total; q += blockDim.x) {
-        const int rank = (int)bufB[q];
+        const int rank = (int)spare[q];
         atomicAdd(&s_count[rank], seg_start[q + 1] - seg_start[q]);
         atomicAdd(&s_segc[rank], 1);
     }
@@ -235,8 +254,13 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
         const cudaError_t e = allow_max_dynamic_smem(index_kernel, attr_done);
         if (e != cudaSuccess) return e;
     }
-    const int threads = n <= 2048 ? 256 : 1024;
-    const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * 256 * sizeof(int);
+    // the largest key is the base rows' 6 A: its bit count picks the passes;
+    // a 512-digit pass needs a thread per digit
+    int key_bits = 1;
+    while (key_bits < 16 && ((uint32_t)RANK_BASE * (uint32_t)max_adapters >> key_bits) != 0u) ++key_bits;
+    const int threads = n <= 2048 ? (key_bits == 9 ? 512 : 256) : 1024;
+    const int digits = key_bits == 9 ? 512 : 256;
+    const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * digits * sizeof(int);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
@@ -248,7 +272,7 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, index_kernel, ids, n, method_tab, max_adapters, perm, aid_s,
-                              seg_start, seg_aid, meta, status, seg_unit, seg_tile);
+                              seg_start, seg_aid, meta, status, seg_unit, seg_tile, key_bits);
 }
 
 }  // namespace scute

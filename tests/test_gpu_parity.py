@@ -59,7 +59,12 @@ def _index_ctx(scute, A):
 
 
 @pytest.mark.parametrize("n,A", [(1, 8), (7, 8), (64, 40), (300, 40), (2049, 1024), (8772, 40),
-                                 (16384, 1024)])
+                                 (16384, 1024),
+                                 # the sort's pass plans: keys below 6 A + 1 take one 8-bit pass up
+                                 # to A = 42, one 9-bit pass up to A = 85 (512 threads from 2048
+                                 # tokens down), two 8-bit passes beyond
+                                 (700, 42), (300, 64), (2048, 85), (2049, 48), (8772, 48),
+                                 (16384, 85), (2048, 86)])
 def test_index_bit_exact(scute, n, A):
     ctx, methods = _index_ctx(scute, A)
     g = np.random.default_rng(n * 31 + A)
