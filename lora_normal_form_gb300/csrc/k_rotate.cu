@@ -101,13 +101,15 @@ __global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bflo
     const int row0 = blockIdx.y * 32 + warp * 4;
     uint4 xv[4];
     int ad[4];
-    // every load of the warp's 4 rows is issued before any is used
+    // every load of the warp's 4 rows is issued before any is used; x is read
+    // once (cache-streaming), so that x', which the shrinks and the GEMM read
+    // next, keeps its place in L2
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int i = row0 + r;
         ad[r] = i < n ? aid_s[i] : -2;
         xv[r] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < n && colok) xv[r] = *reinterpret_cast<const uint4 *>(x + (size_t)perm[i] * d_in + col);
+        if (i < n && colok) xv[r] = __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)perm[i] * d_in + col));
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
