@@ -222,10 +222,14 @@ scute_status scute_linear_batch(scute_ctx *ctx, const scute_call *calls, int n_c
 /* scute_linear_batch with HOST buffers (every x and out, and adapter_ids, in
  * host memory): the inputs are copied into context-owned device staging, the
  * batch runs, the outputs are copied back, all enqueued on `stream`.  When
- * every input (or every output) buffer is pinned and mapped, one kernel
- * launch moves all of them through their device addresses; otherwise each
- * buffer is one asynchronous copy.  The caller synchronises the stream before
- * reading the outputs. */
+ * every input buffer is pinned and mapped, one kernel launch moves all of
+ * them through their device addresses; otherwise each is one asynchronous
+ * copy.  A bf16-context batch of at most 128 tokens whose output buffers are
+ * all pinned, mapped and 16-byte aligned has its outputs stored straight
+ * into them by the step (unless the separate s pass of scute_set_variant is
+ * on); other pinned, mapped outputs take one scatter launch after the batch,
+ * and any other output one copy each.  The caller synchronises the stream
+ * before reading the outputs. */
 scute_status scute_linear_batch_host(scute_ctx *ctx, const scute_call *calls, int n_calls,
                                      const int32_t *ids_host, int64_t n, scute_dtype out_dtype,
                                      void *stream);

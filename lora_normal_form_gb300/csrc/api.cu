@@ -1265,6 +1265,18 @@ scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int 
         dev[i].x = reinterpret_cast<uint8_t *>(c->step_hx) + (size_t)i * STEP_MAX_TOKENS * c->step_hx_cols * c->esz;
         dev[i].out = reinterpret_cast<uint8_t *>(c->step_hout) + (size_t)i * STEP_MAX_TOKENS * c->step_hout_cols * 4;
     }
+    // Pinned, mapped, 16-byte-aligned output buffers take the step's output
+    // stores directly (the step only stores to out, once per element, so
+    // those writes cross to host memory while the step still streams
+    // weights); not with the separate s pass, which reads out back
+    bool direct_out = (c->variant & VARIANT_S_PASS) == 0;
+    void *hout[SCUTE_MAX_CALLS];
+    for (int i = 0; direct_out && i < n_calls; ++i) {
+        hout[i] = const_cast<void *>(mapped_host(calls[i].out));
+        if (!hout[i] || (reinterpret_cast<uintptr_t>(hout[i]) & 15)) direct_out = false;
+    }
+    if (direct_out)
+        for (int i = 0; i < n_calls; ++i) dev[i].out = hout[i];
     // Pinned, mapped host buffers are moved by one gather launch before the
     // step and one scatter launch after it (the device reads and writes them
     // through their device addresses); any other host buffer, by one copy
@@ -1304,6 +1316,7 @@ scute_status scute_linear_batch_host(scute_ctx *c, const scute_call *calls, int 
     }
     s = step_launch(c, dev, n_calls, c->st_ids, (int)n, out_dtype == SCUTE_FP32 ? 1 : 0, st);
     if (s) return s;
+    if (direct_out) return SCUTE_OK;
     // the output buffers are looked up while the step runs
     for (int i = 0; scatter && i < n_calls; ++i) {
         const LayerRec &L = c->layers[calls[i].layer];

@@ -481,13 +481,15 @@ def test_linear_host_matches_linear(scute):
     ctx.close()
 
 
-@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("pinned", [True, "unaligned_out", False])
 @pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
 def test_linear_batch_host_matches_linear_batch(scute, pinned, out_dtype):
     """scute_linear_batch_host over several layers: pinned host buffers go
-    through one gather launch before the step and one scatter launch after it,
-    pageable ones through a copy each; both equal the device-buffer call bit
-    for bit."""
+    through one gather launch before the step, which then stores the outputs
+    straight into the (16-byte-aligned) pinned output buffers; pinned outputs
+    that are not 16-byte aligned through one scatter launch after the step;
+    pageable buffers through a copy each.  All equal the device-buffer call
+    bit for bit."""
     w = _small_decode(n=40)
     names = list(SMALL_NAMES)
     ctx = H.make_ctx(scute, w)
@@ -506,12 +508,19 @@ def test_linear_batch_host_matches_linear_batch(scute, pinned, out_dtype):
         ids_h = ids_h.pin_memory()
         xs = {nm: t.pin_memory() for nm, t in xs.items()}
         outs_h = {nm: t.pin_memory() for nm, t in outs_h.items()}
+    if pinned == "unaligned_out":
+        # each output one element into a pinned buffer of its own
+        for nm in names:
+            d = w.layer(nm).d_out
+            big = torch.empty(w.n * d + 8, dtype=dt).pin_memory()
+            outs_h[nm] = big[1:1 + w.n * d].view(w.n, d)
+            assert outs_h[nm].data_ptr() % 16 != 0
     n0 = ctx.launch_count()
     ctx.linear_batch_host([(xs[nm], ctx.layer_ids[nm], outs_h[nm]) for nm in names], ids_h, out_dtype,
                           stream=torch.cuda.current_stream())
     torch.cuda.synchronize()
-    # the step, plus the gather and the scatter launch for pinned buffers
-    assert ctx.launch_count() - n0 == (3 if pinned else 1)
+    # the step; pinned: plus the gather, and the scatter for unaligned outputs
+    assert ctx.launch_count() - n0 == {True: 2, "unaligned_out": 3, False: 1}[pinned]
     assert ctx.sync_status() == 0
     for nm in names:
         assert torch.equal(outs_h[nm], outs_dev[nm].cpu()), nm
