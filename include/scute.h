@@ -186,8 +186,11 @@ scute_status scute_linear(scute_ctx *ctx, const void *x, const int32_t *adapter_
 
 /* scute_linear with HOST buffers: copies x and adapter_ids from host memory
  * into context-owned device staging, runs scute_linear and copies `out` back,
- * all enqueued on `stream`.  Pinned host memory keeps it asynchronous; the
- * caller synchronises the stream before reading `out_host`. */
+ * all enqueued on `stream`; a bf16-context batch of at most 128 tokens stores
+ * into a pinned, mapped, 16-byte-aligned `out_host` directly (unless the
+ * separate s pass of scute_set_variant is on).  Pinned host memory keeps it
+ * asynchronous; the caller synchronises the stream before reading
+ * `out_host`. */
 scute_status scute_linear_host(scute_ctx *ctx, const void *x_host, const int32_t *ids_host,
                                int64_t n, int layer, void *out_host, scute_dtype out_dtype,
                                void *stream);

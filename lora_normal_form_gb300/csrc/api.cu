@@ -1196,6 +1196,13 @@ scute_status scute_linear_host(scute_ctx *c, const void *x_host, const int32_t *
     const size_t osz = out_dtype == SCUTE_FP32 ? 4 : 2;
     CU_TRY(c, cudaMemcpyAsync(c->st_x, x_host, (size_t)n * L.d_in * c->esz, cudaMemcpyHostToDevice, st));
     CU_TRY(c, cudaMemcpyAsync(c->st_ids, ids_host, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+    // a bf16 decode batch (one step launch, which only stores to out) writes
+    // a pinned, mapped, 16-byte-aligned output buffer directly
+    if (c->dtype != SCUTE_FP32 && n <= STEP_MAX_TOKENS && (c->variant & VARIANT_S_PASS) == 0) {
+        void *dout = const_cast<void *>(mapped_host(out_host));
+        if (dout && (reinterpret_cast<uintptr_t>(dout) & 15) == 0)
+            return scute_linear(c, c->st_x, c->st_ids, n, layer, dout, out_dtype, stream);
+    }
     scute_status s = scute_linear(c, c->st_x, c->st_ids, n, layer, c->st_out, out_dtype, stream);
     if (s) return s;
     CU_TRY(c, cudaMemcpyAsync(out_host, c->st_out, (size_t)n * L.d_out * osz, cudaMemcpyDeviceToHost, st));

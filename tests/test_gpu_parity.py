@@ -466,14 +466,20 @@ def test_n_zero_is_a_no_op(scute):
     ctx.close()
 
 
-def test_linear_host_matches_linear(scute):
+@pytest.mark.parametrize("pinned_out", [True, False])
+def test_linear_host_matches_linear(scute, pinned_out):
+    """scute_linear_host on a decode batch: a pinned output buffer is stored
+    into by the step directly, a pageable one copied back; both equal the
+    device-buffer call bit for bit."""
     w = _small_decode(n=24)
     ctx = H.make_ctx(scute, w)
     outs = H.run_layers(ctx, w, ["up"], "bf16")
     L = w.layer("up")
     x_host = torch.from_numpy(L.get("x").view(np.int16)).view(torch.bfloat16).pin_memory()
     ids_host = torch.from_numpy(w.ids.copy()).pin_memory()
-    out_host = torch.empty(w.n, L.d_out, dtype=torch.bfloat16).pin_memory()
+    out_host = torch.empty(w.n, L.d_out, dtype=torch.bfloat16)
+    if pinned_out:
+        out_host = out_host.pin_memory()
     ctx.linear_host(x_host, ids_host, ctx.layer_ids["up"], out_host, "bf16",
                     stream=torch.cuda.current_stream())
     torch.cuda.synchronize()
