@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     uint32_t *bufA = sm;
     uint32_t *bufB = sm + n;
     int *hist = reinterpret_cast<int *>(bufB + n);
+    // the method table follows the counters of the widest pass this launch runs
+    int8_t *s_tab = reinterpret_cast<int8_t *>(hist + (blockDim.x >> 5) * (key_bits == 9 ? 512 : 256));
     __shared__ int s_warp[33];
     __shared__ int s_count[N_RANKS], s_segc[N_RANKS];
     __shared__ int s_bad;
@@ -134,21 +136,24 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     if (tid == 0) s_bad = 0;
     if (tid < N_RANKS) { s_count[tid] = 0; s_segc[tid] = 0; }
     const uint32_t base_key = (uint32_t)RANK_BASE * (uint32_t)A;
-    // every id of this thread is requested, then every method-table entry:
-    // two rounds of loads instead of two per id
-    // ids per thread, at most: n <= 2048 runs 256 or 512 threads, larger n 1024
+    // the method table and every id of this thread are requested together
+    // (one round of global loads), the ids' methods then read from shared
+    // memory.  ids per thread, at most: n <= 2048 runs 256 or 512 threads,
+    // larger n 1024
     constexpr int PER_T = INDEX_MAX_TOKENS / 1024;
     static_assert(PER_T * 256 >= 2048, "ids per thread for the 256-thread launch");
     int idv[PER_T], mv[PER_T];
+    for (int e = tid; e < A; e += blockDim.x) s_tab[e] = method_tab[e];
 #pragma unroll
     for (int j = 0; j < PER_T; ++j) {
         const int t = tid + j * (int)blockDim.x;
         idv[j] = t < n ? ids[t] : -1;
     }
+    __syncthreads();
 #pragma unroll
     for (int j = 0; j < PER_T; ++j) {
         mv[j] = -1;
-        if (idv[j] >= 0 && idv[j] < A) mv[j] = method_tab[idv[j]];
+        if (idv[j] >= 0 && idv[j] < A) mv[j] = s_tab[idv[j]];
     }
 #pragma unroll
     for (int j = 0; j < PER_T; ++j) {
@@ -214,23 +219,31 @@ __global__ void __launch_bounds__(1024) index_kernel(const int32_t *ids, int n, 
     }
     __syncthreads();
     // work units of the segmented kernels: each segment cut into chunks of
-    // `rows` rows; out[s] = chunks of the segments before s
-    auto unit_prefix = [&](int *out, int rows) {
+    // SEG_UNIT_ROWS and of SEG_TILE_ROWS rows; seg_unit[s] / seg_tile[s] =
+    // chunks of the segments before s.  Both counts share one scan, packed
+    // in 16-bit halves (each total is below n / 32 + n <= 16896)
+    if (seg_unit || seg_tile) {
+        static_assert(INDEX_MAX_TOKENS / SEG_UNIT_ROWS + INDEX_MAX_TOKENS < (1 << 15), "packed unit counts");
+        auto chunks = [&](int q) {
+            const int rows = seg_start[q + 1] - seg_start[q];
+            return (rows + SEG_UNIT_ROWS - 1) / SEG_UNIT_ROWS + (((rows + SEG_TILE_ROWS - 1) / SEG_TILE_ROWS) << 16);
+        };
         const int per_s = (total + blockDim.x - 1) / blockDim.x;
         const int s0 = min(total, tid * per_s), s1 = min(total, s0 + per_s);
         int u = 0;
-        for (int q = s0; q < s1; ++q) u += (seg_start[q + 1] - seg_start[q] + rows - 1) / rows;
+        for (int q = s0; q < s1; ++q) u += chunks(q);
         int tot_u = 0;
         int ex = block_excl_scan(u, s_warp, &tot_u);
         for (int q = s0; q < s1; ++q) {
-            out[q] = ex;
-            ex += (seg_start[q + 1] - seg_start[q] + rows - 1) / rows;
+            if (seg_unit) seg_unit[q] = ex & 0xFFFF;
+            if (seg_tile) seg_tile[q] = ex >> 16;
+            ex += chunks(q);
         }
-        if (tid == 0) out[total] = tot_u;
-        __syncthreads();   // s_warp is reused by the next prefix
-    };
-    if (seg_unit) unit_prefix(seg_unit, SEG_UNIT_ROWS);
-    if (seg_tile) unit_prefix(seg_tile, SEG_TILE_ROWS);
+        if (tid == 0) {
+            if (seg_unit) seg_unit[total] = tot_u & 0xFFFF;
+            if (seg_tile) seg_tile[total] = tot_u >> 16;
+        }
+    }
     if (tid == 0) {
         meta->n_seg = total;
         int off = 0;
@@ -260,7 +273,8 @@ cudaError_t launch_index(const int32_t *ids, int n, const int8_t *method_tab, in
     while (key_bits < 16 && ((uint32_t)RANK_BASE * (uint32_t)max_adapters >> key_bits) != 0u) ++key_bits;
     const int threads = n <= 2048 ? (key_bits == 9 ? 512 : 256) : 1024;
     const int digits = key_bits == 9 ? 512 : 256;
-    const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * digits * sizeof(int);
+    const size_t smem = (size_t)2 * n * sizeof(uint32_t) + (size_t)(threads / 32) * digits * sizeof(int) +
+                        (((size_t)max_adapters + 15) & ~(size_t)15);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);

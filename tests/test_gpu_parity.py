@@ -533,6 +533,34 @@ def test_linear_batch_host_matches_linear_batch(scute, pinned, out_dtype):
     ctx.close()
 
 
+def test_linear_batch_host_s_pass_keeps_staged_outputs(scute):
+    """With DoRA's / (IA)^3's s in a launch of its own (which reads out back),
+    pinned outputs are not the step's out pointers: the batch is gather, step,
+    s pass and scatter, and its outputs equal the device-buffer call with the
+    same placement bit for bit."""
+    w = _small_decode(n=40)
+    names = list(SMALL_NAMES)
+    ctx = H.make_ctx(scute, w)
+    ctx.set_variant(2)
+    ids_dev = torch.from_numpy(w.ids.copy()).cuda()
+    xs = {nm: torch.from_numpy(w.layer(nm).get("x").view(np.int16)).view(torch.bfloat16) for nm in names}
+    outs_dev = {nm: torch.empty(w.n, w.layer(nm).d_out, dtype=torch.bfloat16, device="cuda") for nm in names}
+    ctx.linear_batch([(xs[nm].cuda(), ctx.layer_ids[nm], outs_dev[nm]) for nm in names], ids_dev, "bf16")
+    torch.cuda.synchronize()
+    ids_h = torch.from_numpy(w.ids.copy()).pin_memory()
+    xs_h = {nm: t.pin_memory() for nm, t in xs.items()}
+    outs_h = {nm: torch.empty(w.n, w.layer(nm).d_out, dtype=torch.bfloat16).pin_memory() for nm in names}
+    n0 = ctx.launch_count()
+    ctx.linear_batch_host([(xs_h[nm], ctx.layer_ids[nm], outs_h[nm]) for nm in names], ids_h, "bf16",
+                          stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert ctx.launch_count() - n0 == 4
+    assert ctx.sync_status() == 0
+    for nm in names:
+        assert torch.equal(outs_h[nm], outs_dev[nm].cpu()), nm
+    ctx.close()
+
+
 def test_cuda_graph_replay_matches_eager(scute):
     w = _small_decode(n=40)
     ctx = H.make_ctx(scute, w)
