@@ -83,11 +83,14 @@ __global__ void __launch_bounds__(256) gather_rotate_kernel(const T *__restrict_
     }
 }
 
-// bf16 contexts: one warp per sorted row and 256-column chunk, lane l moving
-// columns [8l, 8l + 8) with one 16-byte load and store; a rotated row's lanes
-// compute their block outputs with rotate_lane (oft_lane.cuh), reading R
-// through L1, where the rows of one adapter that the same CTA handles find it
-// again.  No shared memory and no barrier: every row is independent.
+// bf16 contexts: one warp per sorted row, which it moves whole, eight 256-column
+// chunks at a time (lane l holds columns [8l, 8l + 8) of each chunk as one
+// 16-byte word, so every load of the eight is in flight before the first
+// store, and a row's bytes are read and written in one pass); a rotated row's
+// lanes compute their block outputs with rotate_lane (oft_lane.cuh), reading
+// R through L1.  No shared memory and no barrier: every row is independent.
+// x is read once (cache-streaming), so that x', which the shrinks and the GEMM
+// read next, keeps its place in L2.
 __global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bfloat16 *__restrict__ x, int d_in,
                                                                  int n, const int *__restrict__ perm,
                                                                  const int *__restrict__ aid_s,
@@ -96,30 +99,30 @@ __global__ void __launch_bounds__(256) gather_rotate_bf16_kernel(const __nv_bflo
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col = blockIdx.x * 256 + lane * 8;
-    const bool colok = col < d_in;     // d_in is a multiple of 32: a block's 4 lanes agree
-    const int row0 = blockIdx.y * 32 + warp * 4;
-    uint4 xv[4];
-    int ad[4];
-    // every load of the warp's 4 rows is issued before any is used; x is read
-    // once (cache-streaming), so that x', which the shrinks and the GEMM read
-    // next, keeps its place in L2
+    const int i = blockIdx.x * 8 + warp;
+    if (i >= n) return;   // whole warps; no barrier below
+    const int a = aid_s[i];
+    const __nv_bfloat16 *Rt = a >= 0 ? reinterpret_cast<const __nv_bfloat16 *>(slots[a].Rt) : nullptr;
+    const __nv_bfloat16 *src = x + (size_t)perm[i] * d_in;
+    __nv_bfloat16 *dst = xs + (size_t)i * kdim;
+    const int nch = (d_in + 255) / 256;
+    for (int c0 = 0; c0 < nch; c0 += 8) {
+        uint4 xv[8];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = row0 + r;
-        ad[r] = i < n ? aid_s[i] : -2;
-        xv[r] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < n && colok) xv[r] = __ldcs(reinterpret_cast<const uint4 *>(x + (size_t)perm[i] * d_in + col));
-    }
+        for (int u = 0; u < 8; ++u) {
+            const int col = (c0 + u) * 256 + lane * 8;
+            xv[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (c0 + u < nch && col < d_in) xv[u] = __ldcs(reinterpret_cast<const uint4 *>(src + col));
+        }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = row0 + r;
-        if (i >= n) break;   // uniform across the warp
-        const __nv_bfloat16 *Rt =
-            ad[r] >= 0 ? reinterpret_cast<const __nv_bfloat16 *>(slots[ad[r]].Rt) : nullptr;
-        uint4 o = xv[r];
-        if (Rt != nullptr) o = rotate_lane(xv[r], Rt, col, colok);
-        if (colok) *reinterpret_cast<uint4 *>(xs + (size_t)i * kdim + col) = o;
+        for (int u = 0; u < 8; ++u) {
+            if (c0 + u >= nch) break;   // uniform across the warp
+            const int col = (c0 + u) * 256 + lane * 8;
+            const bool colok = col < d_in;
+            uint4 o = xv[u];
+            if (Rt != nullptr) o = rotate_lane(xv[u], Rt, col, colok);
+            if (colok) *reinterpret_cast<uint4 *>(dst + col) = o;
+        }
     }
 }
 
@@ -141,7 +144,7 @@ cudaError_t launch_gather_rotate(bool f32, const void *x, int d_in, int n, const
     if (f32)
         return cudaLaunchKernelEx(&cfg, gather_rotate_kernel<float>, (const float *)x, d_in, n, perm,
                                   aid_s, slots, (float *)xs, kdim, rows);
-    cfg.gridDim = dim3((unsigned)((d_in + 255) / 256), (unsigned)((n + 31) / 32), 1);
+    cfg.gridDim = dim3((unsigned)((n + 7) / 8), 1, 1);
     return cudaLaunchKernelEx(&cfg, gather_rotate_bf16_kernel, (const __nv_bfloat16 *)x, d_in, n, perm, aid_s,
                               slots, (__nv_bfloat16 *)xs, kdim);
 }
